@@ -1,0 +1,469 @@
+// Grouped FP8 block-scaled GEMM over per-expert token segments, sm_103a.
+//
+//   D[r, n] = BF16( sum_k A[r, k] sA[r, k/128] * B_e[n, k] sB_e[n/128, k/128] )
+//   for every expert e and row r of its segment.
+//
+// Sources: "GEMM 执行方式" §4.1 (P independent problems), §4.4 (Y_e = X_e W_e^T);
+// "AsymGEMM" README ("K-outer, M-inner Loop": a weight tile is fetched once
+// and reused for all token tiles of its expert; "asymScheduler": CTAs own
+// (N-tile, expert) work with no atomics; "Token Layout Protocols");
+// DeepGEMM FP8 article "补偿机制二" (the tensor core applies the UE8M0 block
+// scales itself, selected by a scale-factor id in the instruction descriptor).
+//
+// GB300 design (not the pages' kernels):
+// * swap-AB: the MMA's M = 128 rows are WEIGHT rows (an N-tile of the output)
+//   and the MMA's N dimension is the expert's TOKENS (16..256, step 16), so
+//   a segment of 8 tokens costs a 128 x 16 MMA instead of a padded 128 x 128;
+// * one CTA per SM, persistent; work item = (expert, N-tile, token chunk),
+//   chunks fastest so concurrent CTAs share the weight tile in L2;
+// * warp roles: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner,
+//   warps 2-5 epilogue, warps 6-9 scale-factor loaders;
+// * operands: K-major, 128-byte swizzled tiles of 128 K (TMA), STAGES-deep
+//   mbarrier ring; accumulator 128 lanes x TOK fp32 columns in TMEM;
+// * scales: kind::mxf8f6f4 block scaling with one UE8M0 per row per 32 K;
+//   our 128-wide blocks use one byte for all four K-steps of a block: the
+//   int32 word holding four consecutive blocks is written to TMEM once per
+//   512 K and the byte is picked with sf_id = k_block % 4;
+// * epilogue: tcgen05.ld 32 columns (tokens) per thread row (weight row),
+//   transposed through shared memory into 64-byte row segments of D.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "host_utils.h"
+
+namespace bsf {
+namespace {
+
+constexpr int kBlockW = 128;        // weight rows per tile (MMA M)
+constexpr int kBlockK = 128;        // K per pipeline stage (one 128-byte swizzle row of FP8)
+constexpr int kMaxExperts = 1024;
+constexpr int kSfSlots = 4;
+constexpr int kThreads = 320;
+constexpr int kTmaRows = 32;        // token rows per TMA box
+
+struct GemmArgs {
+  const int32_t* seg_start;  // contiguous: [E+1]; masked: nullptr
+  const int32_t* counts;     // rows per expert (counts / masked_m)
+  int64_t max_m;             // masked slot stride (0 for contiguous)
+  int64_t m_rows;            // rows of A and D
+  const int32_t* sfa;
+  int64_t sfa_ld;
+  const int32_t* sfb;        // [E][nw][N]
+  uint16_t* d;
+  int E, N, K;
+  int* err;
+};
+
+template <int TOK>
+struct Cfg {
+  static constexpr int kStages = TOK <= 64 ? 8 : 4;
+  static constexpr int kAccBufs = TOK <= 128 ? 2 : 1;
+  static constexpr int kSfCols = TOK <= 64 ? 8 : 16;          // 4 weight-SF columns + TOK/32 token-SF columns
+  static constexpr int kSfBase = kAccBufs * TOK;
+  static constexpr int kTmemUsed = kSfBase + kSfSlots * kSfCols;
+  static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
+                                   : kTmemUsed <= 256 ? 256 : 512;
+  static constexpr int kStageB = kBlockW * kBlockK;           // bytes
+  static constexpr int kStageA = TOK * kBlockK;
+  static constexpr int kEpiBytes = 4 * 32 * 32 * 2;           // per epilogue warp: 32 tokens x 32 columns bf16
+  static constexpr int kTableBytes = (3 * kMaxExperts + 4) * 4;
+  static constexpr int kBarBytes = 256;
+  static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kStageB + kStageA) + kEpiBytes +
+                                  kTableBytes + kBarBytes;
+  static_assert(kTmemUsed <= 512, "TMEM budget");
+  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(TOK % 32 == 0 && TOK <= 256, "token tile");
+};
+
+struct Tile {
+  int e, nt, tok0, ntok;
+};
+
+__device__ __forceinline__ Tile decode_tile(int t, const int* tile_start, const int* row0, const int* cnt, int E,
+                                            int nnt, int tok) {
+  int lo = 0, hi = E - 1;   // last expert whose first tile is <= t (never an empty one)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int local = t - tile_start[lo];
+  const int nchunks = (cnt[lo] + tok - 1) / tok;
+  const int nt = local / nchunks;
+  const int chunk = local - nt * nchunks;
+  Tile r;
+  r.e = lo;
+  r.nt = nt;
+  r.tok0 = row0[lo] + chunk * tok;
+  r.ntok = min(tok, cnt[lo] - chunk * tok);
+  return r;
+}
+
+// Bounded wait that ignores the abort flag (used while draining at exit).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// Wait in every lane of a warp; the warp proceeds only if all lanes saw the
+// phase complete, so the .sync.aligned tcgen05 ops that follow stay uniform.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+  const bool ok = mbar_wait(bar, parity, abort, err);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int TOK>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_a,
+                        const GemmArgs p) {
+  using C = Cfg<TOK>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_b = smem;
+  uint8_t* stage_a = stage_b + C::kStages * C::kStageB;
+  uint8_t* epi = stage_a + C::kStages * C::kStageA;
+  int* tile_start = reinterpret_cast<int*>(epi + C::kEpiBytes);
+  int* exp_row0 = tile_start + kMaxExperts + 1;
+  int* exp_cnt = exp_row0 + kMaxExperts;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(tile_start) + C::kTableBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = full + C::kStages;
+  uint64_t* sf_full = empty + C::kStages;
+  uint64_t* sf_empty = sf_full + kSfSlots;
+  uint64_t* acc_full = sf_empty + kSfSlots;
+  uint64_t* acc_empty = acc_full + C::kAccBufs;
+  uint64_t* mma_done = acc_empty + C::kAccBufs;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int E = p.E, N = p.N;
+  const int nnt = N / kBlockW;
+  const int nkb = p.K / kBlockK;
+  const int nw = (nkb + 3) / 4;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < kSfSlots; ++s) {
+      mbar_init(&sf_full[s], 4);
+      mbar_init(&sf_empty[s], 1);
+    }
+    for (int s = 0; s < C::kAccBufs; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], 4);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmap_b);
+    tma_prefetch_desc(&tmap_a);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 2) {
+    // per-expert rows and tile offsets (exclusive scan over experts, 32 at a time)
+    int carry = 0;
+    int bad = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      int row0 = 0, cnt = 0;
+      if (e < E) {
+        cnt = p.counts[e];
+        if (p.seg_start == nullptr) {
+          row0 = static_cast<int>(e * p.max_m);
+          if (cnt < 0 || cnt > p.max_m) { bad = 1; cnt = cnt < 0 ? 0 : static_cast<int>(p.max_m); }
+        } else {
+          row0 = p.seg_start[e];
+          if (cnt < 0 || row0 < 0 || static_cast<int64_t>(row0) + cnt > p.m_rows) { bad = 1; cnt = 0; }
+        }
+        exp_row0[e] = row0;
+        exp_cnt[e] = cnt;
+      }
+      const int ntiles = ((cnt + TOK - 1) / TOK) * nnt;
+      int incl = ntiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (e < E) tile_start[e] = carry + incl - ntiles;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tile_start[E] = carry;
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && blockIdx.x == 0) raise_error(p.err, BSF_DEVERR_SEGMENT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = tile_start[E];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
+        const int n_loads = (tl.ntok + kTmaRows - 1) / kTmaRows;
+        const uint32_t bytes = C::kStageB + n_loads * kTmaRows * kBlockK;
+        const int wrow = tl.e * N + tl.nt * kBlockW;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          tma_load_2d(stage_b + stage * C::kStageB, &tmap_b, &full[stage], kb * kBlockK, wrow);
+          for (int i = 0; i < n_loads; ++i)
+            tma_load_2d(stage_a + stage * C::kStageA + i * kTmaRows * kBlockK, &tmap_a, &full[stage], kb * kBlockK,
+                        tl.tok0 + i * kTmaRows);
+          ++issued;
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // make sure no TMA write is still in flight when the CTA exits
+      const int outstanding = issued < C::kStages ? issued : C::kStages;
+      for (int j = 0; j < outstanding; ++j) {
+        if (stage == 0) { stage = C::kStages; phase ^= 1u; }
+        --stage;
+        drain_wait(&full[stage], phase);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, sf_slot = 0, sf_phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
+        const uint32_t mma_n = (tl.ntok + 15) & ~15;
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * TOK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if ((kb & 3) == 0) {
+            if (!mbar_wait(&sf_full[sf_slot], sf_phase, abort_flag, p.err)) { ok = false; break; }
+          }
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sfw = tmem_base + C::kSfBase + sf_slot * C::kSfCols;
+          const uint32_t sft = sfw + 4;
+          const uint32_t idesc = idesc_mxf8_e4m3(kBlockW, mma_n, kb & 3, kb & 3);
+          const uint64_t adesc = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB));
+          const uint64_t bdesc = smem_desc_k_sw128(smem_u32(stage_a + stage * C::kStageA));
+#pragma unroll
+          for (int k = 0; k < kBlockK / 32; ++k) {
+            // advance 32 bytes (one K=32 step of FP8) inside the swizzled 128-byte rows
+            mma_mxf8(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sfw, sft, (kb | k) != 0);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+          if ((kb & 3) == 3 || kb == nkb - 1) {
+            tc_commit(&sf_empty[sf_slot]);
+            if (++sf_slot == kSfSlots) { sf_slot = 0; sf_phase ^= 1u; }
+          }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[acc]);
+        if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
+      }
+      // wait for every MMA issued by this thread before TMEM can be released
+      tc_commit(mma_done);
+      drain_wait(mma_done, 0);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                       // TMEM lane quadrant = weight rows 32q..32q+31
+    uint16_t* buf = reinterpret_cast<uint16_t*>(epi) + (warp - 2) * 32 * 32;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
+      if (!warp_wait(&acc_full[acc], acc_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * TOK;
+      const int ncol = (tl.ntok + 31) & ~31;
+      for (int c0 = 0; c0 < ncol; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_x32(taddr + c0, r);
+        tmem_wait_ld();
+        // buf[j][lane] = D[token c0 + j][weight row 32q + lane]
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(r[j]));
+          buf[j * 32 + lane] = *reinterpret_cast<const uint16_t*>(&h);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int j = (lane >> 2) + 8 * i;
+          if (c0 + j < tl.ntok) {
+            const uint4 v = *reinterpret_cast<const uint4*>(buf + j * 32 + (lane & 3) * 8);
+            uint16_t* dst = p.d + static_cast<int64_t>(tl.tok0 + c0 + j) * N + tl.nt * kBlockW + 32 * q +
+                            (lane & 3) * 8;
+            *reinterpret_cast<uint4*>(dst) = v;
+          }
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
+    }
+  } else {
+    // ------------------------------------------------------------ scale-factor loaders
+    // Each of the four warps writes the same SF words into its own TMEM lane
+    // quadrant: column c of a block holds rows (lane + 32 c), byte j = K-block 4g + j.
+    const int q = warp & 3;
+    uint32_t sf_slot = 0, sf_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
+      const int mma_n = (tl.ntok + 15) & ~15;
+      const int32_t* sfb_base = p.sfb + static_cast<int64_t>(tl.e) * nw * N + tl.nt * kBlockW + lane;
+      for (int g = 0; g < nw; ++g) {
+        uint32_t w[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) w[c] = static_cast<uint32_t>(__ldg(sfb_base + static_cast<int64_t>(g) * N + 32 * c));
+        uint32_t a[TOK / 32];
+#pragma unroll
+        for (int c = 0; c < TOK / 32; ++c) {
+          const int rl = lane + 32 * c;
+          const int64_t row = static_cast<int64_t>(tl.tok0) + rl;
+          a[c] = (rl < mma_n && row < p.m_rows) ? static_cast<uint32_t>(__ldg(p.sfa + g * p.sfa_ld + row))
+                                                 : 0x7F7F7F7Fu;
+        }
+        if (!warp_wait(&sf_empty[sf_slot], sf_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t col = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::kSfBase + sf_slot * C::kSfCols;
+        tmem_st_x4(col, w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int c = 0; c < TOK / 32; c += 2) tmem_st_x2(col + 4 + c, a[c], a[c + 1]);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_full[sf_slot]);
+        if (++sf_slot == kSfSlots) { sf_slot = 0; sf_phase ^= 1u; }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D uint8 tensor [rows, cols] (row pitch = cols bytes), box {128 cols, box_rows}, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  const cuuint32_t box[2] = {128u, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int TOK>
+bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int64_t max_tiles, cudaStream_t s) {
+  using C = Cfg<TOK>;
+  CUtensorMap map_a, map_b;
+  if (!make_map(&map_a, a, args.m_rows, args.K, kTmaRows)) return BSF_ERR_CUDA;
+  if (!make_map(&map_b, b, static_cast<int64_t>(args.E) * args.N, args.K, kBlockW)) return BSF_ERR_CUDA;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::kSmem)) != cudaSuccess)
+      return BSF_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  int64_t grid = sm_count();
+  if (max_tiles < grid) grid = max_tiles;
+  if (grid <= 0) return BSF_OK;
+  grouped_gemm_kernel<TOK><<<static_cast<unsigned>(grid), kThreads, C::kSmem, s>>>(map_b, map_a, args);
+  return launch_status();
+}
+
+bsf_status check_common(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, int64_t m_rows, const uint8_t* b,
+                        const int32_t* sfb, const void* d, int64_t E, int64_t N, int64_t K, int flags) {
+  if (E <= 0 || E > kMaxExperts || N <= 0 || K <= 0 || N % 128 || K % 128) return BSF_ERR_INVALID_ARGUMENT;
+  if (flags & ~BSF_B_HOST_MAPPED) return BSF_ERR_INVALID_ARGUMENT;
+  if (!a || !sfa || !b || !sfb || !d) return BSF_ERR_INVALID_ARGUMENT;
+  if (sfa_ld < m_rows || sfa_ld % 4) return BSF_ERR_INVALID_ARGUMENT;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(d) || !aligned16(sfa) || !aligned16(sfb))
+    return BSF_ERR_MISALIGNED;
+  if (m_rows > INT32_MAX || E * N > INT32_MAX || K > (1 << 24)) return BSF_ERR_UNSUPPORTED;
+  return BSF_OK;
+}
+
+}  // namespace
+}  // namespace bsf
+
+using namespace bsf;
+
+extern "C" bsf_status bsf_grouped_gemm_contig(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, int64_t m_cap,
+                                              const uint8_t* b, const int32_t* sfb, void* d,
+                                              const int32_t* seg_start, const int32_t* counts, int64_t E, int64_t N,
+                                              int64_t K, int flags, bsf_stream_t stream) {
+  if (m_cap <= 0) return m_cap == 0 ? BSF_OK : BSF_ERR_INVALID_ARGUMENT;
+  const bsf_status st = check_common(a, sfa, sfa_ld, m_cap, b, sfb, d, E, N, K, flags);
+  if (st != BSF_OK) return st;
+  if (!seg_start || !counts) return BSF_ERR_INVALID_ARGUMENT;
+  int* err = device_error_ptr();
+  if (!err) return BSF_ERR_CUDA;
+  GemmArgs args{seg_start, counts, 0, m_cap, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
+                static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err};
+  const int64_t max_tiles = (m_cap / 256 + E) * (N / 128);
+  return launch<256>(args, a, b, max_tiles, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" bsf_status bsf_grouped_gemm_masked(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, const uint8_t* b,
+                                              const int32_t* sfb, void* d, const int32_t* masked_m, int64_t E,
+                                              int64_t max_m, int64_t N, int64_t K, int64_t expected_m, int flags,
+                                              bsf_stream_t stream) {
+  if (max_m <= 0) return BSF_ERR_INVALID_ARGUMENT;
+  const int64_t m_rows = E * max_m;
+  const bsf_status st = check_common(a, sfa, sfa_ld, m_rows, b, sfb, d, E, N, K, flags);
+  if (st != BSF_OK) return st;
+  if (!masked_m) return BSF_ERR_INVALID_ARGUMENT;
+  int* err = device_error_ptr();
+  if (!err) return BSF_ERR_CUDA;
+  GemmArgs args{nullptr, masked_m, max_m, m_rows, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
+                static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t hint = expected_m > 0 ? expected_m : max_m;
+  if (max_m <= 64 || hint <= 64) {
+    const int64_t max_tiles = E * ((max_m + 63) / 64) * (N / 128);
+    return launch<64>(args, a, b, max_tiles, s);
+  }
+  const int64_t max_tiles = E * ((max_m + 255) / 256) * (N / 128);
+  return launch<256>(args, a, b, max_tiles, s);
+}

@@ -1,0 +1,298 @@
+// Deterministic top-k routing: per-expert counts, segment offsets, stable
+// ranks, inverse index, and the scatter of quantised rows into the packed
+// operand of the grouped GEMM.
+//
+// "GEMM 执行方式" (rainlin-net) §4.2-§4.3 (topk_ids, M_e, packed rows,
+// m_indices, output_index) and §4.6 (A-aligned segments; ep_scatter copies
+// each valid route's token and records its row).  "CuTeDSL bei Perplexity",
+// MoE dispatch: count tokens per expert, give each a unique index inside its
+// expert, then copy rows into (optionally padded) buffers with a wide grid.
+//
+// Unlike an atomic scatter (whose order inside an expert is arbitrary, §4.6),
+// ranks here are stable in the flat assignment index t * k_r + r, so every
+// output is bit-reproducible:
+//   route_count   per-chunk expert histograms          (grid: chunks of 2048 assignments)
+//   route_scan    per-expert prefix over chunks, M_e, aligned segment starts (1 CTA)
+//   route_assign  stable ranks -> output_index, token_of_row (grid: chunks)
+//   route_fill    per packed row: padding marks, m_indices, row + SF copy (grid: rows)
+#include "common.cuh"
+#include "host_utils.h"
+
+namespace bsf {
+namespace {
+
+constexpr int kChunk = 2048;           // assignments per CTA in count / assign
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;  // each warp owns kChunk / kWarps consecutive assignments
+constexpr int kSub = kChunk / kWarps;  // 256
+constexpr int kMaxExperts = 1024;
+
+__global__ void __launch_bounds__(kThreads) route_count_kernel(const int32_t* __restrict__ ids, int64_t R, int E,
+                                                               int32_t* __restrict__ blk_counts, int* err) {
+  __shared__ int hist[kMaxExperts];
+  __shared__ int bad;
+  for (int e = threadIdx.x; e < E; e += kThreads) hist[e] = 0;
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunk;
+  for (int j = threadIdx.x; j < kChunk; j += kThreads) {
+    const int64_t i = base + j;
+    if (i >= R) break;
+    const int id = ids[i];
+    if (id >= E) bad = 1;
+    else if (id >= 0) atomicAdd(&hist[id], 1);   // counts only: order does not matter
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kThreads) blk_counts[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
+  if (threadIdx.x == 0 && bad) raise_error(err, BSF_DEVERR_EXPERT_ID);
+}
+
+// Single CTA of 1024 threads (one expert per thread; E <= 1024).
+__global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ blk_counts, int nblk, int E, int layout,
+                                                          int64_t align_or_max_m, int64_t m_cap,
+                                                          int32_t* __restrict__ counts, int32_t* __restrict__ seg_start,
+                                                          int* err) {
+  __shared__ int warp_sums[32];
+  const int e = threadIdx.x;
+  int64_t M = 0;
+  if (e < E) {
+    for (int b = 0; b < nblk; ++b) {
+      const int64_t idx = static_cast<int64_t>(b) * E + e;
+      const int c = blk_counts[idx];
+      blk_counts[idx] = static_cast<int32_t>(M);   // exclusive prefix over chunks
+      M += c;
+    }
+  }
+  if (layout == BSF_LAYOUT_MASKED) {
+    if (e < E) {
+      const int64_t placed = M < align_or_max_m ? M : align_or_max_m;
+      counts[e] = static_cast<int32_t>(placed);
+      seg_start[e] = static_cast<int32_t>(e * align_or_max_m);
+      if (M > align_or_max_m) raise_error(err, BSF_DEVERR_MASKED_OVERFLOW);
+    }
+    if (e == 0) seg_start[E] = static_cast<int32_t>(E * align_or_max_m);
+    return;
+  }
+  // contiguous: exclusive scan of the aligned segment lengths over experts
+  const int64_t len = e < E ? (M + align_or_max_m - 1) / align_or_max_m * align_or_max_m : 0;
+  int64_t incl = len;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = static_cast<int>(incl);
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += v;
+    }
+    warp_sums[lane] = s;
+  }
+  __syncthreads();
+  const int64_t warp_prefix = warp > 0 ? warp_sums[warp - 1] : 0;
+  const int64_t excl = warp_prefix + incl - len;
+  if (e < E) {
+    counts[e] = static_cast<int32_t>(M);
+    seg_start[e] = static_cast<int32_t>(excl);
+  }
+  if (e == E - 1) {
+    seg_start[E] = static_cast<int32_t>(excl + len);
+    if (excl + len > m_cap) raise_error(err, BSF_DEVERR_SEGMENT);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) route_assign_kernel(const int32_t* __restrict__ ids, int64_t R, int kr,
+                                                                int E, int layout, int64_t max_m, int64_t m_cap,
+                                                                const int32_t* __restrict__ blk_base,
+                                                                const int32_t* __restrict__ seg_start,
+                                                                int32_t* __restrict__ output_index,
+                                                                int32_t* __restrict__ token_of_row, int* err) {
+  extern __shared__ int smem[];
+  int* warp_cnt = smem;                       // [kWarps][E]
+  int* seg = smem + kWarps * E;               // [E]
+  __shared__ int overflow;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int j = threadIdx.x; j < kWarps * E; j += kThreads) warp_cnt[j] = 0;
+  for (int e = threadIdx.x; e < E; e += kThreads) seg[e] = seg_start[e];
+  if (threadIdx.x == 0) overflow = 0;
+  __syncthreads();
+
+  const int64_t sub0 = static_cast<int64_t>(blockIdx.x) * kChunk + warp * kSub;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  // pass 1: per-warp histogram of its sub-chunk
+  for (int r = 0; r < kSub; r += 32) {
+    const int64_t i = sub0 + r + lane;
+    int id = i < R ? ids[i] : -1;
+    const bool valid = id >= 0 && id < E;
+    const int key = valid ? id : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    if (valid && (peers & lt_mask) == 0) warp_cnt[warp * E + id] += __popc(peers);
+  }
+  __syncthreads();
+  // exclusive prefix over the warps, on top of this chunk's base per expert
+  for (int e = threadIdx.x; e < E; e += kThreads) {
+    int run = blk_base[static_cast<int64_t>(blockIdx.x) * E + e];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = warp_cnt[w * E + e];
+      warp_cnt[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  // pass 2: stable rank = warp base + earlier matches in this warp's sub-chunk
+  for (int r = 0; r < kSub; r += 32) {
+    const int64_t i = sub0 + r + lane;
+    const int id = i < R ? ids[i] : -1;
+    const bool valid = id >= 0 && id < E;
+    const int key = valid ? id : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    int rank = 0;
+    if (valid) rank = warp_cnt[warp * E + id] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (valid && (peers & lt_mask) == 0) warp_cnt[warp * E + id] += __popc(peers);
+    __syncwarp();
+    if (i < R) {
+      int64_t dest = -1;
+      if (valid) {
+        if (layout == BSF_LAYOUT_MASKED) {
+          if (rank < max_m) dest = static_cast<int64_t>(id) * max_m + rank;
+        } else {
+          dest = static_cast<int64_t>(seg[id]) + rank;
+        }
+        if (dest >= m_cap) {
+          dest = -1;
+          overflow = 1;
+        }
+      }
+      output_index[i] = static_cast<int32_t>(dest);
+      if (dest >= 0) token_of_row[dest] = static_cast<int32_t>(i / kr);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && overflow) raise_error(err, BSF_DEVERR_SEGMENT);
+}
+
+constexpr int kFillRows = 32;   // packed rows per CTA in route_fill
+
+// Per packed row r < seg_start[E]: mark padding rows (token -1), write
+// m_indices, copy the token's FP8 row and SF words (zeros / bytes 127 for padding).
+__global__ void __launch_bounds__(kThreads) route_fill_kernel(int E, int64_t m_cap, const int32_t* __restrict__ counts,
+                                                              const int32_t* __restrict__ seg_start,
+                                                              int32_t* __restrict__ token_of_row,
+                                                              int32_t* __restrict__ m_indices,
+                                                              const uint8_t* __restrict__ q,
+                                                              const int32_t* __restrict__ sf, int64_t sf_ld, int64_t K,
+                                                              uint8_t* __restrict__ a_packed,
+                                                              int32_t* __restrict__ sfa_packed, int64_t sfa_ld) {
+  __shared__ int tok[kFillRows];
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kFillRows;
+  const int64_t rows_used = seg_start[E];
+  if (row0 >= rows_used || row0 >= m_cap) return;
+  if (threadIdx.x < kFillRows) {
+    const int64_t r = row0 + threadIdx.x;
+    int t = -2;                                  // -2: outside the used rows
+    if (r < rows_used && r < m_cap) {
+      int lo = 0, hi = E - 1;                    // last expert with seg_start[e] <= r
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (seg_start[mid] <= r) lo = mid; else hi = mid - 1;
+      }
+      // skip empty segments that share the start
+      const bool pad = r - seg_start[lo] >= counts[lo];
+      if (pad) {
+        token_of_row[r] = -1;
+        t = -1;
+      } else {
+        t = token_of_row[r];
+      }
+      if (m_indices) m_indices[r] = lo;
+    }
+    tok[threadIdx.x] = t;
+  }
+  __syncthreads();
+  if (q == nullptr) return;
+  // SF words: thread (word i, row) with consecutive rows -> coalesced stores
+  const int64_t n_words = (K + 511) / 512;
+  for (int64_t j = threadIdx.x; j < n_words * kFillRows; j += kThreads) {
+    const int64_t i = j / kFillRows;
+    const int rl = static_cast<int>(j % kFillRows);
+    const int t = tok[rl];
+    if (t == -2) continue;
+    sfa_packed[i * sfa_ld + row0 + rl] = t >= 0 ? sf[i * sf_ld + t] : 0x7F7F7F7F;
+  }
+  // FP8 rows: one warp per row, 16-byte vectors
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nvec = K / 16;
+  for (int rl = warp; rl < kFillRows; rl += kWarps) {
+    const int t = tok[rl];
+    if (t == -2) continue;
+    uint4* dst = reinterpret_cast<uint4*>(a_packed + (row0 + rl) * K);
+    if (t >= 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(q + static_cast<int64_t>(t) * K);
+      for (int64_t v = lane; v < nvec; v += 32) dst[v] = __ldg(src + v);
+    } else {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int64_t v = lane; v < nvec; v += 32) dst[v] = z;
+    }
+  }
+}
+
+}  // namespace
+}  // namespace bsf
+
+using namespace bsf;
+
+extern "C" size_t bsf_route_workspace_bytes(int64_t T, int64_t kr, int64_t E) {
+  if (T < 0 || kr <= 0 || E <= 0) return 0;
+  const int64_t R = T * kr;
+  const int64_t nblk = (R + kChunk - 1) / kChunk;
+  return static_cast<size_t>((nblk > 0 ? nblk : 1) * E * sizeof(int32_t));
+}
+
+extern "C" bsf_status bsf_route(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout,
+                                int64_t align_or_max_m, int32_t* counts, int32_t* seg_start, int32_t* output_index,
+                                int32_t* token_of_row, int32_t* m_indices, int64_t m_cap, const uint8_t* q,
+                                const int32_t* sf, int64_t sf_ld, int64_t K, uint8_t* a_packed, int32_t* sfa_packed,
+                                int64_t sfa_ld, void* workspace, size_t workspace_bytes, bsf_stream_t stream) {
+  if (T < 0 || kr <= 0 || E <= 0 || E > kMaxExperts) return BSF_ERR_INVALID_ARGUMENT;
+  if (layout != BSF_LAYOUT_CONTIGUOUS && layout != BSF_LAYOUT_MASKED) return BSF_ERR_INVALID_ARGUMENT;
+  if (align_or_max_m < 1) return BSF_ERR_INVALID_ARGUMENT;
+  if (!counts || !seg_start || !output_index || !token_of_row) return BSF_ERR_INVALID_ARGUMENT;
+  const int64_t R = T * kr;
+  const int64_t need_cap = layout == BSF_LAYOUT_MASKED ? E * align_or_max_m : R + E * (align_or_max_m - 1);
+  if (m_cap < need_cap || m_cap > INT32_MAX) return BSF_ERR_INVALID_ARGUMENT;
+  if (R > INT32_MAX) return BSF_ERR_UNSUPPORTED;
+  if (workspace_bytes < bsf_route_workspace_bytes(T, kr, E) || !workspace) return BSF_ERR_INVALID_ARGUMENT;
+  if (q) {
+    if (!sf || !a_packed || !sfa_packed || K <= 0 || K % 128) return BSF_ERR_INVALID_ARGUMENT;
+    if (sf_ld < T || sf_ld % 4 || sfa_ld < m_cap || sfa_ld % 4) return BSF_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(a_packed) || !aligned16(sf) || !aligned16(sfa_packed)) return BSF_ERR_MISALIGNED;
+  }
+  int* err = device_error_ptr();
+  if (!err) return BSF_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int nblk = static_cast<int>((R + kChunk - 1) / kChunk);
+  int32_t* blk = static_cast<int32_t*>(workspace);
+  const int e32 = static_cast<int>(E);
+  if (nblk > 0) {
+    route_count_kernel<<<nblk, kThreads, 0, s>>>(topk_ids, R, e32, blk, err);
+  }
+  route_scan_kernel<<<1, 1024, 0, s>>>(blk, nblk, e32, layout, align_or_max_m, m_cap, counts, seg_start, err);
+  if (nblk > 0) {
+    const size_t smem = static_cast<size_t>(kWarps + 1) * E * sizeof(int);
+    route_assign_kernel<<<nblk, kThreads, smem, s>>>(topk_ids, R, static_cast<int>(kr), e32, layout, align_or_max_m,
+                                                     m_cap, blk, seg_start, output_index, token_of_row, err);
+  }
+  const int64_t fill_blocks = (m_cap + kFillRows - 1) / kFillRows;
+  if (fill_blocks > 0) {
+    route_fill_kernel<<<static_cast<unsigned>(fill_blocks), kThreads, 0, s>>>(
+        e32, m_cap, counts, seg_start, token_of_row, m_indices, q, sf, sf_ld, K, a_packed, sfa_packed, sfa_ld);
+  }
+  return launch_status();
+}

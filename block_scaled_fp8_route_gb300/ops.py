@@ -1,0 +1,157 @@
+"""Thin torch-facing binding of the C ABI (argument marshalling only).
+
+Every function here allocates its outputs with torch (device memory is the
+only thing torch provides), passes raw pointers and the current CUDA stream to
+``libbsfroute.so`` and returns the tensors.  All arithmetic runs in the CUDA
+kernels.  Names follow the C entry points without the ``bsf_`` prefix.
+"""
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+CONTIGUOUS = 0
+MASKED = 1
+B_HOST_MAPPED = 1
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def sf_ld(rows: int) -> int:
+    """Row stride (int32 words) of a packed MN-major SF tensor: rows rounded up to 4."""
+    return (rows + 3) // 4 * 4
+
+
+def sf_words(K: int) -> int:
+    return (K // 128 + 3) // 4
+
+
+def device_error(clear: bool = True, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _lib.check(_lib.load().bsf_get_device_error(ctypes.byref(code), int(clear), _stream(stream)), "get_device_error")
+    return code.value
+
+
+def quantise_act(x, q=None, sf=None, stream=None):
+    """x bf16 [T, K] -> (q uint8 [T, K], sf int32 [ceil(K/512), sf_ld(T)])."""
+    T, K = x.shape
+    x = x.contiguous()
+    if q is None:
+        q = torch.empty((T, K), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty((sf_words(K), sf_ld(T)), dtype=torch.int32, device=x.device)
+    _lib.check(_lib.load().bsf_quantise_act(_ptr(x), T, K, _ptr(q), _ptr(sf), sf.shape[1], _stream(stream)),
+               "quantise_act")
+    return q, sf
+
+
+def quantise_weight(w, stream=None):
+    """w bf16 [E, N, K] -> (q uint8 [E, N, K], sf128 float32 [E, N/128, K/128])."""
+    E, N, K = w.shape
+    w = w.contiguous()
+    q = torch.empty((E, N, K), dtype=torch.uint8, device=w.device)
+    sf128 = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device=w.device)
+    _lib.check(_lib.load().bsf_quantise_weight(_ptr(w), E, N, K, _ptr(q), _ptr(sf128), _stream(stream)),
+               "quantise_weight")
+    return q, sf128
+
+
+def prepare_weight_sf(sf128, K: int, stream=None):
+    """sf128 float32 [E, N/128, K/128] -> per-row packed int32 [E, ceil(K/512), N]."""
+    E, nb, _ = sf128.shape
+    N = nb * 128
+    sfb = torch.empty((E, sf_words(K), N), dtype=torch.int32, device=sf128.device)
+    _lib.check(_lib.load().bsf_prepare_weight_sf(_ptr(sf128.contiguous()), E, N, K, _ptr(sfb), _stream(stream)),
+               "prepare_weight_sf")
+    return sfb
+
+
+def route_capacity(T: int, kr: int, E: int, layout: int, align_or_max_m: int) -> int:
+    """Worst-case packed row count (no device-to-host sync needed)."""
+    if layout == MASKED:
+        return E * align_or_max_m
+    return T * kr + E * (align_or_max_m - 1)
+
+
+class RouteBuffers:
+    """Preallocated outputs of ``route`` (reused across steps)."""
+
+    def __init__(self, T, kr, E, layout, align_or_max_m, K=0, device="cuda", scatter=True):
+        self.T, self.kr, self.E, self.layout, self.align_or_max_m, self.K = T, kr, E, layout, align_or_max_m, K
+        self.m_cap = route_capacity(T, kr, E, layout, align_or_max_m)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.counts = torch.empty(E, **i32)
+        self.seg_start = torch.empty(E + 1, **i32)
+        self.output_index = torch.empty((T, kr), **i32)
+        self.token_of_row = torch.empty(max(self.m_cap, 1), **i32)
+        self.m_indices = torch.empty(max(self.m_cap, 1), **i32)
+        ws = _lib.load().bsf_route_workspace_bytes(T, kr, E)
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        if scatter and K:
+            self.a_packed = torch.empty((max(self.m_cap, 1), K), dtype=torch.uint8, device=device)
+            self.sfa_packed = torch.empty((sf_words(K), sf_ld(self.m_cap)), dtype=torch.int32, device=device)
+        else:
+            self.a_packed = self.sfa_packed = None
+
+
+def route(topk_ids, E, layout, align_or_max_m, q=None, sf=None, bufs=None, stream=None):
+    """Routing + optional scatter; returns a RouteBuffers holding every output."""
+    T, kr = topk_ids.shape
+    K = q.shape[1] if q is not None else 0
+    if bufs is None:
+        bufs = RouteBuffers(T, kr, E, layout, align_or_max_m, K=K, device=topk_ids.device, scatter=q is not None)
+    lib = _lib.load()
+    _lib.check(lib.bsf_route(
+        _ptr(topk_ids.contiguous()), T, kr, E, layout, align_or_max_m,
+        _ptr(bufs.counts), _ptr(bufs.seg_start), _ptr(bufs.output_index), _ptr(bufs.token_of_row),
+        _ptr(bufs.m_indices), bufs.m_cap,
+        _ptr(q), _ptr(sf), sf.shape[1] if sf is not None else 0, K,
+        _ptr(bufs.a_packed) if q is not None else None, _ptr(bufs.sfa_packed) if q is not None else None,
+        bufs.sfa_packed.shape[1] if (q is not None and bufs.sfa_packed is not None) else 0,
+        _ptr(bufs.workspace), bufs.workspace.numel(), _stream(stream)), "route")
+    return bufs
+
+
+def grouped_gemm_contig(a, sfa, b, sfb, seg_start, counts, d=None, flags=0, stream=None):
+    """a uint8 [m_cap, K], b uint8 [E, N, K] -> d bf16 [m_cap, N] (segment rows written)."""
+    m_cap, K = a.shape
+    E, N, _ = b.shape
+    if d is None:
+        d = torch.empty((m_cap, N), dtype=torch.bfloat16, device=a.device)
+    _lib.check(_lib.load().bsf_grouped_gemm_contig(
+        _ptr(a), _ptr(sfa), sfa.shape[1], m_cap, _ptr(b), _ptr(sfb), _ptr(d), _ptr(seg_start), _ptr(counts),
+        E, N, K, flags, _stream(stream)), "grouped_gemm_contig")
+    return d
+
+
+def grouped_gemm_masked(a, sfa, b, sfb, masked_m, max_m, d=None, expected_m=0, flags=0, stream=None):
+    """a uint8 [E*max_m, K] (or [E, max_m, K]), b uint8 [E, N, K] -> d bf16 [E*max_m, N]."""
+    K = a.shape[-1]
+    E, N, _ = b.shape
+    if d is None:
+        d = torch.empty((E * max_m, N), dtype=torch.bfloat16, device=a.device)
+    _lib.check(_lib.load().bsf_grouped_gemm_masked(
+        _ptr(a), _ptr(sfa), sfa.shape[1], _ptr(b), _ptr(sfb), _ptr(d), _ptr(masked_m), E, max_m, N, K,
+        expected_m, flags, _stream(stream)), "grouped_gemm_masked")
+    return d
+
+
+def combine(y, output_index, topk_weights, z=None, stream=None):
+    """y bf16 [rows, N] -> z bf16 [T, N]."""
+    rows, N = y.shape
+    T, kr = output_index.shape
+    if z is None:
+        z = torch.empty((T, N), dtype=torch.bfloat16, device=y.device)
+    _lib.check(_lib.load().bsf_combine(
+        _ptr(y), rows, _ptr(output_index.contiguous()), _ptr(topk_weights.contiguous()), T, kr, N, _ptr(z),
+        _stream(stream)), "combine")
+    return z

@@ -1,0 +1,67 @@
+"""One pass of the MoE expert path on resident buffers.
+
+    x bf16 [T, K] --quantise_act--> (q, sf) --route(+scatter)--> packed A
+      --grouped GEMM (contiguous or masked)--> y bf16 --combine--> z bf16 [T, N]
+
+with an optional second grouped GEMM (the down projection, K2 x N2) on a
+separately supplied packed bf16 input that shares the routing; then the
+combine reads the second GEMM's output.  Weights are quantised once at
+construction (``quantise_weight`` + ``prepare_weight_sf``).  Every step is a
+``libbsfroute.so`` call; this class only owns buffers and orders the calls on
+one stream.
+"""
+
+import torch
+
+from . import ops
+
+
+class MoEPath:
+    def __init__(self, E, kr, T, K, N, w_bf16, layout=ops.CONTIGUOUS, align_or_max_m=1, w2_bf16=None,
+                 device="cuda", weights_on_host=False, expected_m=0):
+        self.E, self.kr, self.T, self.K, self.N = E, kr, T, K, N
+        self.layout, self.align_or_max_m = layout, align_or_max_m
+        self.expected_m = expected_m
+        self.flags = ops.B_HOST_MAPPED if weights_on_host else 0
+        self.wq, sf128 = ops.quantise_weight(w_bf16.to(device))
+        self.sfb = ops.prepare_weight_sf(sf128, K)
+        if weights_on_host:
+            self.wq = self.wq.cpu().pin_memory()
+            self.sfb = self.sfb.cpu().pin_memory()
+        self.two_gemms = w2_bf16 is not None
+        if self.two_gemms:
+            _, self.N2, self.K2 = w2_bf16.shape
+            self.w2q, sf2 = ops.quantise_weight(w2_bf16.to(device))
+            self.sfb2 = ops.prepare_weight_sf(sf2, self.K2)
+        self.bufs = ops.RouteBuffers(T, kr, E, layout, align_or_max_m, K=K, device=device)
+        m = self.bufs.m_cap
+        self.q = torch.empty((T, K), dtype=torch.uint8, device=device)
+        self.sf = torch.empty((ops.sf_words(K), ops.sf_ld(T)), dtype=torch.int32, device=device)
+        self.y = torch.empty((max(m, 1), N), dtype=torch.bfloat16, device=device)
+        if self.two_gemms:
+            self.q2 = torch.empty((max(m, 1), self.K2), dtype=torch.uint8, device=device)
+            self.sf2 = torch.empty((ops.sf_words(self.K2), ops.sf_ld(m)), dtype=torch.int32, device=device)
+            self.y2 = torch.empty((max(m, 1), self.N2), dtype=torch.bfloat16, device=device)
+            self.z = torch.empty((T, self.N2), dtype=torch.bfloat16, device=device)
+        else:
+            self.z = torch.empty((T, N), dtype=torch.bfloat16, device=device)
+
+    def gemm(self, a, sfa, wq, sfb, d):
+        b = self.bufs
+        if self.layout == ops.MASKED:
+            return ops.grouped_gemm_masked(a, sfa, wq, sfb, b.counts, self.align_or_max_m, d=d,
+                                           expected_m=self.expected_m, flags=self.flags)
+        return ops.grouped_gemm_contig(a, sfa, wq, sfb, b.seg_start, b.counts, d=d, flags=self.flags)
+
+    def step(self, x, topk_ids, topk_weights, h2=None):
+        """Run the whole path; ``h2`` is the packed bf16 [m_cap, K2] input of the second GEMM."""
+        ops.quantise_act(x, q=self.q, sf=self.sf)
+        ops.route(topk_ids, self.E, self.layout, self.align_or_max_m, q=self.q, sf=self.sf, bufs=self.bufs)
+        self.gemm(self.bufs.a_packed, self.bufs.sfa_packed, self.wq, self.sfb, self.y)
+        out = self.y
+        if self.two_gemms:
+            ops.quantise_act(h2, q=self.q2, sf=self.sf2)
+            self.gemm(self.q2, self.sf2, self.w2q, self.sfb2, self.y2)
+            out = self.y2
+        ops.combine(out, self.bufs.output_index, topk_weights, z=self.z)
+        return self.z

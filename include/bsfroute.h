@@ -1,0 +1,207 @@
+/*
+ * bsfroute — FP8 block-scaled MoE routing + grouped GEMM for GB300 (sm_103a).
+ *
+ * C ABI of the hot path:
+ *   quantise_act  -> route (+ scatter) -> grouped_gemm_{contig,masked} -> combine
+ * plus the once-per-weight-load steps quantise_weight and prepare_weight_sf.
+ *
+ * Conventions of every entry point
+ *   - Pointers are DEVICE pointers (CUDA global memory) unless a parameter says
+ *     otherwise.  The caller allocates and owns every buffer; no entry point
+ *     allocates memory.
+ *   - `stream` is a cudaStream_t (0 = legacy default stream).  All work is
+ *     enqueued on it; calls never synchronise the device.
+ *   - Arguments are validated on the host before anything is enqueued; a bad
+ *     argument returns a non-zero bsf_status and enqueues nothing.
+ *   - Problems found while the kernels run (an expert id >= E, a masked slot
+ *     overflow, a weight scale that is not a power of two, a wait that ran
+ *     out) set bits of a sticky device error word; read it with
+ *     bsf_get_device_error.
+ *   - bf16 is IEEE bfloat16 stored as uint16; e4m3 is FP8 E4M3 ("e4m3fn":
+ *     bias 7, max 448, no infinities) stored as uint8.
+ *
+ * Scale-factor (SF) format (DeepGEMM FP8 article, nxmr.cn, sections
+ * "补偿机制一" and "补偿机制三"): every scale is an exact power of two 2**e,
+ * stored as a UE8M0 byte e + 127; four bytes are packed per int32, byte j
+ * (bits 8j..8j+7) holding K-block 4i + j of word i (K-blocks of 128).  Packed
+ * SF tensors are MN-major: element [i][row] at offset i * ld + row, with ld
+ * (in int32 words) a multiple of 4 (16 bytes, the TMA-aligned stride).
+ */
+#ifndef BSFROUTE_H
+#define BSFROUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* bsf_stream_t; /* same type as cudaStream_t */
+
+typedef enum bsf_status {
+  BSF_OK = 0,
+  BSF_ERR_INVALID_ARGUMENT = 1, /* a size, layout or pointer is not acceptable */
+  BSF_ERR_MISALIGNED = 2,       /* a pointer or stride breaks the 16-byte TMA alignment */
+  BSF_ERR_UNSUPPORTED = 3,      /* the shape is valid but not supported by this build */
+  BSF_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed */
+  BSF_ERR_DEVICE = 5            /* the current device is not an sm_100-class GPU */
+} bsf_status;
+
+/* Device error word bits (sticky until cleared). */
+#define BSF_DEVERR_EXPERT_ID 0x1       /* a topk id >= E was seen (route skips it) */
+#define BSF_DEVERR_MASKED_OVERFLOW 0x2 /* masked layout: assignments past max_m were dropped */
+#define BSF_DEVERR_TIMEOUT 0x4         /* a bounded wait ran out; the kernel returned early */
+#define BSF_DEVERR_BAD_SCALE 0x8       /* a weight scale is not a positive power of two */
+#define BSF_DEVERR_SEGMENT 0x10        /* a segment does not fit the A buffer; it was skipped */
+
+/* Layouts of the packed token operand ("AsymGEMM" README, "Token Layout Protocols"). */
+#define BSF_LAYOUT_CONTIGUOUS 0
+#define BSF_LAYOUT_MASKED 1
+
+/* GEMM flags. */
+#define BSF_B_HOST_MAPPED 0x1 /* b / sfb are host pointers to pinned, mapped host memory */
+
+const char* bsf_status_string(bsf_status status);
+int bsf_version(void);
+
+/* Reads the device error word into *code (host pointer) after synchronising
+ * `stream`; clears it when `clear` is non-zero. */
+bsf_status bsf_get_device_error(int32_t* code, int clear, bsf_stream_t stream);
+
+/*
+ * bsf_quantise_act — activations to FP8 with 1 x 128 power-of-two scales.
+ * DeepGEMM article "补偿机制一" (power-of-two SF, UE8M0) and "FP8 的精度陷阱"
+ * (E4M3); recipe (gran_m, gran_k) = (1, 128).
+ *   x     bf16  [T, K] row-major.
+ *   q     e4m3  [T, K] row-major (output).
+ *   sf    int32 [ceil(K/512)][sf_ld] packed MN-major (output); rows >= T are
+ *         not written.  sf_ld >= T, multiple of 4.
+ * For each row t and K-block b: amax = max |x|; e = least integer with
+ * amax <= 448 * 2**e (0 for an all-zero block), clamped to [-126, 127];
+ * q = E4M3_RNE_satfinite(x * 2**-e); SF byte e + 127.
+ * Needs K % 128 == 0, T >= 0.  T == 0 is a no-op.
+ */
+bsf_status bsf_quantise_act(const void* x, int64_t T, int64_t K, uint8_t* q, int32_t* sf, int64_t sf_ld,
+                            bsf_stream_t stream);
+
+/*
+ * bsf_quantise_weight — expert weights to FP8 with 128 x 128 power-of-two scales
+ * (same rule as bsf_quantise_act over 128 x 128 blocks; recipe gran_n = 128).
+ *   w      bf16  [E, N, K] row-major.
+ *   q      e4m3  [E, N, K] (output).
+ *   sf128  fp32  [E, N/128, K/128] (output), every entry 2**e.
+ * Needs N % 128 == 0, K % 128 == 0.
+ */
+bsf_status bsf_quantise_weight(const void* w, int64_t E, int64_t N, int64_t K, uint8_t* q, float* sf128,
+                               bsf_stream_t stream);
+
+/*
+ * bsf_prepare_weight_sf — once per weight load: fp32 128 x 128 scales to the
+ * per-row packed UE8M0 layout the GEMM reads (DeepGEMM article "补偿机制三":
+ * weight SFs are transformed once and reused).
+ *   sf128  fp32  [E, N/128, K/128], each a positive power of two.
+ *   sfb    int32 [E][ceil(K/512)][N] (output): word [e][i][n] packs the bytes
+ *          of K-blocks 4i..4i+3 of row block n / 128; bytes past K/128 are 127.
+ * A scale that is not a power of two sets BSF_DEVERR_BAD_SCALE (its byte is
+ * written as 127).
+ */
+bsf_status bsf_prepare_weight_sf(const float* sf128, int64_t E, int64_t N, int64_t K, int32_t* sfb,
+                                 bsf_stream_t stream);
+
+/*
+ * bsf_route — top-k routing, segment offsets, inverse index, and (optionally)
+ * the scatter of quantised rows into the packed operand.
+ * "GEMM 执行方式" (rainlin-net) §4.2 (topk tensors, R = T k_r = sum M_e),
+ * §4.3 (packed layout, m_indices, output_index), §4.6 (A-aligned segments,
+ * ep_scatter); "CuTeDSL bei Perplexity", MoE dispatch (count per expert,
+ * unique index per token, copy into optionally padded buffers).
+ *   topk_ids      int32 [T, kr]; ids < 0 are dropped routes; ids >= E set
+ *                 BSF_DEVERR_EXPERT_ID and are dropped.
+ *   layout        BSF_LAYOUT_CONTIGUOUS: segment e spans
+ *                 [seg_start[e], seg_start[e+1]), length ceil(M_e/align)*align;
+ *                 BSF_LAYOUT_MASKED: segment e spans [e*max_m, (e+1)*max_m),
+ *                 at most max_m rows, further assignments dropped
+ *                 (BSF_DEVERR_MASKED_OVERFLOW).
+ *   align_or_max_m  align (>= 1) for CONTIGUOUS, max_m (>= 1) for MASKED.
+ *   counts        int32 [E] (output): rows placed per expert (M_e, or
+ *                 min(M_e, max_m) for MASKED) — the GEMM's counts / masked_m.
+ *   seg_start     int32 [E+1] (output).
+ *   output_index  int32 [T, kr] (output): packed row of each assignment, -1 if dropped.
+ *   token_of_row  int32 [m_cap] (output): token of each packed row, -1 for
+ *                 padding rows; rows >= seg_start[E] are not written.
+ *   m_indices     int32 [m_cap] (output, may be NULL): expert owning each
+ *                 packed row < seg_start[E] (padding rows included).
+ *   m_cap         rows of the packed buffers: at least T*kr + E*(align-1)
+ *                 (CONTIGUOUS) or E*max_m (MASKED) — no device-to-host sync
+ *                 is needed to size them.
+ *   q, sf, sf_ld  optional scatter source (NULL: indices only): e4m3 [T, K]
+ *                 and packed SF [ceil(K/512)][sf_ld] from bsf_quantise_act.
+ *   a_packed      e4m3 [m_cap, K] (output): row r = q[token_of_row[r]];
+ *                 padding rows are zero.
+ *   sfa_packed    int32 [ceil(K/512)][sfa_ld] (output), sfa_ld >= m_cap,
+ *                 multiple of 4; padding rows get bytes 127.
+ *   workspace     device scratch of bsf_route_workspace_bytes(T, kr, E) bytes.
+ * Order inside an expert: ascending flat index t*kr + r (stable; the order of
+ * the worked example in §4.3 / §4.6).  Deterministic.
+ */
+size_t bsf_route_workspace_bytes(int64_t T, int64_t kr, int64_t E);
+bsf_status bsf_route(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout, int64_t align_or_max_m,
+                     int32_t* counts, int32_t* seg_start, int32_t* output_index, int32_t* token_of_row,
+                     int32_t* m_indices, int64_t m_cap, const uint8_t* q, const int32_t* sf, int64_t sf_ld,
+                     int64_t K, uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld, void* workspace,
+                     size_t workspace_bytes, bsf_stream_t stream);
+
+/*
+ * bsf_grouped_gemm_contig — D[r, :] = BF16( dequant(A[r, :]) . dequant(B_e)^T )
+ * for every expert e and every row r in [seg_start[e], seg_start[e] + counts[e]).
+ * "GEMM 执行方式" §4.1 (P independent problems), §4.4 (Y_e = X_e W_e^T);
+ * "AsymGEMM" README API reference (m_grouped_fp8_asym_gemm_nt_contiguous:
+ * (data, scale) pairs, NT, bf16 output); DeepGEMM article "补偿机制二"
+ * (block-scaled MMA consumes the UE8M0 scales).
+ *   a        e4m3  [m_cap, K]; sfa int32 [ceil(K/512)][sfa_ld] (1 x 128 SFs).
+ *   b        e4m3  [E, N, K]; sfb int32 [E][ceil(K/512)][N] from bsf_prepare_weight_sf.
+ *   d        bf16  [m_cap, N] (output); only the rows above are written.
+ *   seg_start, counts  int32 [E+1], [E] (device), e.g. from bsf_route.
+ * FP32 accumulation on the tensor cores, round-to-nearest-even to bf16.
+ * Needs N % 128 == 0, K % 128 == 0, 16-byte aligned a, b, d.
+ * flags: BSF_B_HOST_MAPPED — b and sfb live in pinned host memory mapped
+ * into the device address space (the "AsymGEMM" asymmetric memory path);
+ * the kernel reads them directly, nothing is staged in HBM.
+ */
+bsf_status bsf_grouped_gemm_contig(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, int64_t m_cap,
+                                   const uint8_t* b, const int32_t* sfb, void* d, const int32_t* seg_start,
+                                   const int32_t* counts, int64_t E, int64_t N, int64_t K, int flags,
+                                   bsf_stream_t stream);
+
+/*
+ * bsf_grouped_gemm_masked — the same contraction on the masked layout
+ * ("AsymGEMM" README, "Token Layout Protocols": expert g at rows g*max_m,
+ * masked_m[g] valid rows, 0 = inactive; m_grouped_fp8_asym_gemm_nt_masked).
+ *   a    e4m3 [E, max_m, K]; sfa int32 [ceil(K/512)][sfa_ld], sfa_ld >= E*max_m.
+ *   d    bf16 [E, max_m, N] (output); rows >= masked_m[g] are not written.
+ *   masked_m int32 [E] (device), each <= max_m.
+ *   expected_m  hint of the typical masked_m (0: unknown); picks the token tile.
+ */
+bsf_status bsf_grouped_gemm_masked(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, const uint8_t* b,
+                                   const int32_t* sfb, void* d, const int32_t* masked_m, int64_t E, int64_t max_m,
+                                   int64_t N, int64_t K, int64_t expected_m, int flags, bsf_stream_t stream);
+
+/*
+ * bsf_combine — weighted un-permute: z[t, :] = BF16( sum_r p[t, r] * y[output_index[t, r], :] )
+ * "GEMM 执行方式" §4.4 / §4.6 (ep_gather); "CuTeDSL bei Perplexity" (combine
+ * accumulates in registers using the dispatch offsets).
+ *   y             bf16  [y_rows, N] expert outputs (the GEMM's d).
+ *   output_index  int32 [T, kr] from bsf_route; -1 entries are skipped.
+ *   topk_weights  fp32  [T, kr].
+ *   z             bf16  [T, N] (output).
+ * FP32 accumulation in r order, round-to-nearest-even to bf16.  Needs N % 8 == 0.
+ */
+bsf_status bsf_combine(const void* y, int64_t y_rows, const int32_t* output_index, const float* topk_weights,
+                       int64_t T, int64_t kr, int64_t N, void* z, bsf_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSFROUTE_H */

@@ -1,0 +1,49 @@
+"""Helpers for the GPU parity tests: tensor <-> numpy bit views, oracle runs of a
+workload, and the per-expert tolerance check of the grouped GEMM."""
+
+import numpy as np
+import torch
+
+import oracle
+
+
+def bits16(t):
+    """bf16 tensor -> uint16 numpy array of its bit patterns (on the CPU)."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def u8(t):
+    return t.detach().cpu().contiguous().numpy().view(np.uint8)
+
+
+def i32(t):
+    return t.detach().cpu().contiguous().numpy().astype(np.int64)
+
+
+def require_gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from block_scaled_fp8_route_gb300 import build, _lib
+    _lib.load(build.build())
+    return torch.device("cuda:0")
+
+
+def check_expert_block(d_gpu_bits, ref_bits, what):
+    """calc_diff <= 1e-3 and the per-element bound on one expert's valid block."""
+    d = oracle.formats.bf16_bits_to_f64(d_gpu_bits)
+    ref = oracle.formats.bf16_bits_to_f64(ref_bits)
+    assert np.all(np.isfinite(d)), f"{what}: non-finite output"
+    diff = oracle.checks.calc_diff(d, ref)
+    assert diff <= oracle.checks.CALC_DIFF_MAX, f"{what}: calc_diff {diff:.3e}"
+    ok = oracle.checks.elementwise_ok(d, ref)
+    if not ok.all():
+        bad = np.argwhere(~ok)[:5]
+        raise AssertionError(f"{what}: {int((~ok).sum())} elements outside the bound, e.g. "
+                             + ", ".join(f"{tuple(b)}: {d[tuple(b)]} vs {ref[tuple(b)]}" for b in bad))
+    return diff
+
+
+def oracle_packed_operand(aq, asf_bytes, token_of_row):
+    """Oracle scatter of quantised token rows into packed rows (padding: zero data, byte 127)."""
+    rows = oracle.route.scatter_rows(aq, token_of_row)
+    sfb = oracle.route.scatter_rows(asf_bytes, token_of_row, pad_value=127)
+    return rows, sfb

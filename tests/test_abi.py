@@ -1,0 +1,44 @@
+"""CPU-side checks of the C-ABI library: it builds, loads, and exports every
+symbol that include/bsfroute.h declares (no compute calls: no GPU here)."""
+
+import ctypes
+
+import pytest
+
+from block_scaled_fp8_route_gb300 import _lib, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build.build()
+    return _lib.load(path)
+
+
+def test_every_header_symbol_is_exported(lib):
+    names = _lib.header_symbols()
+    assert "bsf_grouped_gemm_contig" in names and "bsf_route" in names
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(_lib.SIGNATURES), "binding signatures out of sync with the header"
+
+
+def test_host_only_calls(lib):
+    assert lib.bsf_version() >= 1
+    assert lib.bsf_status_string(0) == b"ok"
+    assert lib.bsf_status_string(2).startswith(b"pointer")
+    # workspace size is host arithmetic: one int32 per (2048-assignment chunk, expert)
+    assert lib.bsf_route_workspace_bytes(8192, 8, 256) == 32 * 256 * 4
+    assert lib.bsf_route_workspace_bytes(1, 1, 4) == 16
+
+
+def test_argument_validation_needs_no_device(lib):
+    nul = ctypes.c_void_p(0)
+    # K not a multiple of 128 is rejected before anything touches the device
+    assert lib.bsf_quantise_act(nul, 4, 100, nul, nul, 4, nul) == 1
+    # N not a multiple of 128
+    assert lib.bsf_grouped_gemm_contig(nul, nul, 4, 4, nul, nul, nul, nul, nul, 2, 100, 128, 0, nul) == 1
+    # unknown layout
+    assert lib.bsf_route(nul, 4, 2, 4, 7, 1, nul, nul, nul, nul, nul, 8, nul, nul, 0, 0, nul, nul, 0, nul, 0,
+                         nul) == 1
+    # combine with N not a multiple of 8
+    assert lib.bsf_combine(nul, 4, nul, nul, 2, 2, 12, nul, nul) == 1

@@ -1,0 +1,84 @@
+"""GPU parity of the combine kernel and of the whole path (quantise -> route ->
+grouped GEMM -> combine) against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from block_scaled_fp8_route_gb300 import MoEPath, ops
+from tests.gpu_util import bits16, check_expert_block, i32, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_gpu()
+
+
+@pytest.mark.parametrize("T,kr,rows,N", [(1, 1, 4, 8), (77, 8, 700, 3072), (513, 2, 1100, 264)])
+def test_combine_within_one_ulp_of_float64(dev, T, kr, rows, N):
+    g = torch.Generator().manual_seed(T)
+    y = torch.randn(rows, N, generator=g).to(torch.bfloat16)
+    idx = torch.randint(-1, rows, (T, kr), generator=g, dtype=torch.int32)
+    p = torch.rand(T, kr, generator=g)
+    z = ops.combine(y.to(dev), idx.to(dev), p.to(dev))
+    torch.cuda.synchronize()
+    ref = oracle.combine.combine(bits16(y), idx.numpy(), p.numpy())
+    zg = bits16(z).astype(np.int64)
+    # same sign-magnitude ordering: at most one bf16 step apart
+    def ordered(b):
+        b = b.astype(np.int64)
+        return np.where(b & 0x8000, -(b & 0x7FFF), b)
+    assert np.max(np.abs(ordered(zg) - ordered(ref))) <= 1
+
+
+def _oracle_path(x, wt, ids, p, w, a_or_m):
+    aq, asf = oracle.quantise.quantise_act(bits16(x))
+    bq, bsf = oracle.quantise.quantise_weight(bits16(wt))
+    r = oracle.route.route(ids.numpy(), w.E, w.layout, align=w.align if w.layout == W.CONTIGUOUS else 1,
+                           max_m=a_or_m if w.layout == W.MASKED else 0)
+    a_rows = oracle.route.scatter_rows(aq, r["token_of_row"])
+    a_sf = oracle.route.scatter_rows(asf, r["token_of_row"], pad_value=127)
+    y, _ = oracle.gemm.grouped_gemm(a_rows, a_sf, bq, bsf, r["seg_start"], r["counts"])
+    z = oracle.combine.combine(y, r["output_index"], p.numpy())
+    return r, y, z
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_a128", "decode"])
+def test_end_to_end(dev, name):
+    w = W.WORKLOADS[name]
+    x, wt = W.activations(w), W.weights(w)
+    ids, p = W.routing(w)
+    a_or_m = w.max_m if w.layout == W.MASKED else w.align
+    path = MoEPath(w.E, w.kr, w.T, w.K, w.N, wt, layout=w.layout, align_or_max_m=a_or_m, device=dev,
+                   expected_m=w.T * w.kr // w.E)
+    z = path.step(x.to(dev), ids.to(dev), p.to(dev))
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    r, y_ref, z_ref = _oracle_path(x, wt, ids, p, w, a_or_m)
+    assert np.array_equal(i32(path.bufs.output_index), r["output_index"])
+    yg = bits16(path.y)
+    for e in range(w.E):
+        s, c = int(r["seg_start"][e]), int(r["counts"][e])
+        if c:
+            check_expert_block(yg[s:s + c], y_ref[s:s + c], f"{name} expert {e}")
+    check_expert_block(bits16(z), z_ref, f"{name} combined output")
+    # combine of the GPU's own y is within one bf16 step of the float64 combine of that y
+    z_from_gpu_y = oracle.combine.combine(yg, r["output_index"], p.numpy())
+    d = np.abs(oracle.formats.bf16_bits_to_f64(bits16(z)) - oracle.formats.bf16_bits_to_f64(z_from_gpu_y))
+    step = np.abs(oracle.formats.bf16_bits_to_f64(z_from_gpu_y)) * 2.0 ** -7 + 1e-30
+    assert np.all(d <= step)
+
+
+def test_end_to_end_deterministic(dev):
+    w = W.WORKLOADS["decode"]
+    x, wt = W.activations(w), W.weights(w)
+    ids, p = W.routing(w)
+    path = MoEPath(w.E, w.kr, w.T, w.K, w.N, wt, layout=w.layout, align_or_max_m=w.max_m, device=dev)
+    xs, idss, ps = x.to(dev), ids.to(dev), p.to(dev)
+    first = path.step(xs, idss, ps).clone()
+    for _ in range(19):
+        assert torch.equal(path.step(xs, idss, ps).view(torch.int16), first.view(torch.int16))
