@@ -1,0 +1,411 @@
+"""Benchmark of the MoE expert path on one GB300 (or N replicas, one per GPU).
+
+One step = quantise_act -> route (+scatter) -> grouped GEMM(s) -> combine on
+one batch of seeded synthetic inputs already resident in HBM.  Prints ONE JSON
+line (rank 0).  Default workload: the masked decode batch (T=128, top-8 of
+128 experts, K=4096, N=3072, max_m=64), metric HBM GB/s.  ``--workload
+prefill|large`` times the large-M batches (metric TFLOPS).
+
+--impl reference times the CPU oracle (float64 numpy restatement of the same
+path) on a bounded sample of the same workload, on the host cores.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "dram_traffic.json")
+GEMM_SRC = os.path.join(ROOT, "block_scaled_fp8_route_gb300", "csrc", "gemm.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "large", "tiny"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+# ----------------------------------------------------------------------------- work accounting
+def step_work(w, counts, placed_rows):
+    """Algorithmic bytes and GEMM flops of one step (valid rows only; padding excluded)."""
+    T, K, N, E, kr = w.T, w.K, w.N, w.E, w.kr
+    R = T * kr
+    nw = (K // 128 + 3) // 4
+    active = [int(c) for c in counts if c > 0]
+    rows = sum(active)
+    b = {}
+    b["quantise"] = T * K * 2 + T * K + T * nw * 4
+    b["route"] = R * 4 + R * 4 + placed_rows * 8 + rows * (2 * K + 2 * nw * 4)
+    gemm_bytes = len(active) * (N * K + N * nw * 4) + rows * (K + nw * 4 + N * 2)
+    flops = 2.0 * rows * N * K
+    b["gemm"] = gemm_bytes
+    out_n = N
+    if w.K2:
+        nw2 = (w.K2 // 128 + 3) // 4
+        b["quantise2"] = placed_rows * w.K2 * 3 + placed_rows * nw2 * 4
+        b["gemm2"] = len(active) * (w.N2 * w.K2 + w.N2 * nw2 * 4) + rows * (w.K2 + nw2 * 4 + w.N2 * 2)
+        flops += 2.0 * rows * w.N2 * w.K2
+        out_n = w.N2
+    b["combine"] = R * out_n * 2 + T * out_n * 2 + R * 8
+    return b, flops
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- traffic record
+def gemm_source_hash():
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "block_scaled_fp8_route_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it matches this source."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        rec = json.load(f)
+    entry = rec.get(workload)
+    if not entry or entry.get("gemm_source_hash") != gemm_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) leg
+def oracle_sample(w, n_experts, seed=0):
+    """Time the CPU oracle on the path restricted to ``n_experts`` experts (inputs built untimed).
+
+    Returns (seconds, algorithmic bytes, flops, description)."""
+    import oracle
+    rng_t = torch.Generator().manual_seed(seed)
+    wsmall = W.with_tokens(w, w.T)
+    x = W.activations(wsmall)
+    ids, p = W.routing(wsmall)
+    counts = np.bincount(ids.numpy().reshape(-1), minlength=w.E)
+    experts = [int(e) for e in np.argsort(-counts)[:n_experts] if counts[e] > 0]
+    wt = W.weights(w, experts=experts)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    wb = wt.view(torch.int16).numpy().view(np.uint16)
+    bq, bsf = oracle.quantise.quantise_weight(wb)          # weights are prepared once, outside the step
+    del rng_t
+    t0 = time.perf_counter()
+    aq, asf = oracle.quantise.quantise_act(xb)
+    r = oracle.route.route(ids.numpy(), w.E, w.layout, align=w.align, max_m=w.max_m)
+    a_rows = oracle.route.scatter_rows(aq, r["token_of_row"])
+    a_sf = oracle.route.scatter_rows(asf, r["token_of_row"], pad_value=127)
+    y = np.zeros((r["rows_used"], w.N), dtype=np.uint16)
+    rows = 0
+    for i, e in enumerate(experts):
+        s, c = int(r["seg_start"][e]), int(r["counts"][e])
+        y[s:s + c] = oracle.gemm.expert_gemm(a_rows[s:s + c], a_sf[s:s + c], bq[i], bsf[i])
+        rows += c
+    oracle.combine.combine(y, r["output_index"], p.numpy())
+    dt = time.perf_counter() - t0
+    K, N = w.K, w.N
+    nw = (K // 128 + 3) // 4
+    byts = len(experts) * (N * K + N * nw * 4) + rows * (K + nw * 4 + N * 2)
+    flops = 2.0 * rows * N * K
+    desc = (f"oracle over {len(experts)} of {w.E} experts ({rows} routed rows; quantise/route/combine over the "
+            f"whole batch), gate-up GEMM only")
+    return dt, byts, flops, desc
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, w, metric, unit, hib):
+    """--impl reference: the oracle as it stands, on the host cores."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    n_exp = 8 if w.name == "decode" else 2
+    for _ in range(args.warmup):
+        oracle_sample(w, n_exp)
+    tot_t, tot_b, tot_f = 0.0, 0.0, 0.0
+    desc = ""
+    for _ in range(args.steps):
+        dt, b, f, desc = oracle_sample(w, n_exp)
+        tot_t += dt
+        tot_b += b
+        tot_f += f
+    value = (tot_b / tot_t / 1e9) if unit == "GB/s" else (tot_f / tot_t / 1e12)
+    line = {
+        "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+        "higher_is_better": hib, "data": "synthetic", "dtype": "f64",
+        "config": {"workload": w.name},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": host_cores(), "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU leg
+def main():
+    args = parse()
+    w = W.WORKLOADS[args.workload]
+    large_m = w.name in ("prefill", "large")
+    metric = "grouped-GEMM TFLOPS & % FP8 roofline (large M); HBM GB/s & % peak (decode)"
+    unit = "TFLOP/s" if large_m else "GB/s"
+    if args.impl == "reference":
+        run_reference(args, w, metric, unit, True)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    from block_scaled_fp8_route_gb300 import MoEPath, ops, _lib
+    _lib.load()      # fails loudly if the CUDA library was not built
+
+    pk = peaks()
+    ids, p = W.routing(w, device=dev)
+    x = W.activations(w, device=dev)
+    wt = W.weights(w, device=dev)
+    wt2 = W.weights(w, device=dev, N=w.N2, K=w.K2, tag=1) if w.K2 else None
+    a_or_m = w.max_m if w.layout == W.MASKED else w.align
+    expected_m = w.T * w.kr // w.E
+    path = MoEPath(w.E, w.kr, w.T, w.K, w.N, wt, layout=w.layout, align_or_max_m=a_or_m, w2_bf16=wt2,
+                   device=dev, expected_m=expected_m)
+    del wt, wt2
+    torch.cuda.empty_cache()
+    h2 = W.activations(W.with_tokens(w, path.bufs.m_cap), device=dev, K=w.K2, tag=1) if w.K2 else None
+    stream = torch.cuda.current_stream()
+
+    # routing counts for the work accounting (untimed)
+    path.step(x, ids, p, h2)
+    torch.cuda.synchronize()
+    counts = path.bufs.counts.cpu().numpy()
+    placed = int(path.bufs.seg_start[-1].item())
+    assert ops.device_error() == 0, "device error during setup"
+    bytes_by_kernel, flops = step_work(w, counts, placed)
+    step_bytes = sum(bytes_by_kernel.values())
+
+    for _ in range(args.warmup):
+        path.step(x, ids, p, h2)
+
+    # time the GEMM launches with events on the launching stream
+    gemm_events = []
+    orig_gemm = path.gemm
+
+    def timed_gemm(*a, **k):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        r = orig_gemm(*a, **k)
+        e1.record(stream)
+        gemm_events.append((e0, e1))
+        return r
+
+    path.gemm = timed_gemm
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        path.step(x, ids, p, h2)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    path.gemm = orig_gemm
+    elapsed_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = tt.item()
+    assert ops.device_error() == 0, "device error during the timed steps"
+
+    gemm_ms = [a.elapsed_time(b) for a, b in gemm_events]
+    n_gemm_per_step = 2 if w.K2 else 1
+    # dominant kernel: the first (gate-up) GEMM
+    first_gemm_ms = statistics.mean(gemm_ms[0::n_gemm_per_step])
+    launches_per_step = 1 + 4 + 1 + 1 + (2 if w.K2 else 0)
+
+    if large_m:
+        value = flops * args.steps * world / (elapsed_ms / 1e3) / 1e12
+        fp8_peak = 2.0 * pk["bf16_tflops"]           # fp8 dense = 2 x bf16 dense (nominal ratio 4.5 / 2.25)
+        gflops = 2.0 * int(counts.sum()) * w.N * w.K
+        achieved = gflops / (first_gemm_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp8_peak, "peak_src": f"2 x bf16 burst ({pk['src']})"}
+    else:
+        value = step_bytes * args.steps * world / (elapsed_ms / 1e3) / 1e9
+        achieved = bytes_by_kernel["gemm"] / (first_gemm_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "peak_src": pk["src"]}
+    roof["traffic"] = recorded_traffic(w.name)
+    roof["kernel"] = "grouped_gemm_kernel"
+    roof["algorithmic_per_launch"] = bytes_by_kernel["gemm"] if not large_m else 2.0 * int(counts.sum()) * w.N * w.K
+    roof["launch_ms"] = first_gemm_ms
+
+    # ---------------------------------------------------------------- end to end through the public API
+    e2e = None
+    if not args.no_e2e:
+        hx = x.cpu().pin_memory()
+        hids = ids.cpu().pin_memory()
+        hp = p.cpu().pin_memory()
+        hz = torch.empty(path.z.shape, dtype=path.z.dtype).pin_memory()
+        dx, dids, dp = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(p)
+        h2d = hx.numel() * hx.element_size() + hids.numel() * 4 + hp.numel() * 4
+        d2h = hz.numel() * hz.element_size()
+
+        def e2e_step():
+            dx.copy_(hx, non_blocking=True)
+            dids.copy_(hids, non_blocking=True)
+            dp.copy_(hp, non_blocking=True)
+            z = path.step(dx, dids, dp, h2)
+            hz.copy_(z, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = s0.elapsed_time(s1)
+        if world > 1:
+            tt = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            e_ms = tt.item()
+        ev = (flops * args.steps * world / (e_ms / 1e3) / 1e12) if large_m else \
+            (step_bytes * args.steps * world / (e_ms / 1e3) / 1e9)
+        e2e = {"value": ev, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms / args.steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_exp = 16 if w.name == "decode" else 3
+        dt, b, f, desc = oracle_sample(w, n_exp)
+        cv = (f / dt / 1e12) if large_m else (b / dt / 1e9)
+        cpu = {"value": cv, "unit": unit, "cores": host_cores(), "kind": "oracle", "sample": desc,
+               "seconds": dt}
+
+    if rank == 0:
+        cfg = {"workload": w.name, "T": w.T, "top_k": w.kr, "experts": w.E, "K": w.K, "N": w.N,
+               "layout": "masked" if w.layout == W.MASKED else "contiguous",
+               "max_m" if w.layout == W.MASKED else "align": a_or_m,
+               "l2": f"no flush: weights {(w.E * w.N * w.K) / 1e9:.2f} GB > 129 MB L2, streamed each step",
+               "routed_rows": int(counts.sum()), "active_experts": int((counts > 0).sum())}
+        if w.K2:
+            cfg.update({"K2": w.K2, "N2": w.N2})
+        line = {
+            "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 acc -> bf16",
+            "data": "synthetic", "config": cfg,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "gpu_launches": launches_per_step * args.steps,
+            "step_bytes": step_bytes, "step_gemm_flops": flops,
+            "per_kernel_bytes": bytes_by_kernel,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

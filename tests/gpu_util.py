@@ -42,6 +42,23 @@ def check_expert_block(d_gpu_bits, ref_bits, what):
     return diff
 
 
+def check_combined(z_gpu_bits, z_ref_bits, y_ref_bits, output_index, topk_weights, row_rms, what):
+    """Combined output: calc_diff <= 1e-3 and the GEMM bound propagated through the combine."""
+    z = oracle.formats.bf16_bits_to_f64(z_gpu_bits)
+    zr = oracle.formats.bf16_bits_to_f64(z_ref_bits)
+    y = oracle.formats.bf16_bits_to_f64(y_ref_bits)
+    diff = oracle.checks.calc_diff(z, zr)
+    assert diff <= oracle.checks.CALC_DIFF_MAX, f"{what}: calc_diff {diff:.3e}"
+    bound = oracle.checks.combined_bound(zr, y, output_index, topk_weights, row_rms)
+    bad = np.abs(z - zr) > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements outside the propagated bound"
+    return diff
+
+
+def expert_row_rms(y_ref_bits, seg_start, counts):
+    return oracle.checks.expert_row_rms(oracle.formats.bf16_bits_to_f64(y_ref_bits), seg_start, counts)
+
+
 def oracle_packed_operand(aq, asf_bytes, token_of_row):
     """Oracle scatter of quantised token rows into packed rows (padding: zero data, byte 127)."""
     rows = oracle.route.scatter_rows(aq, token_of_row)

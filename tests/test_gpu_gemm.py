@@ -159,8 +159,8 @@ def test_tiny_full(dev):
     _workload_gemm_check(dev, "tiny_a128")
 
 
-def test_decode_full_size(dev):
-    _workload_gemm_check(dev, "decode")
+def test_decode_full_size_sampled(dev):
+    _workload_gemm_check(dev, "decode", n_sample=14)
 
 
 def test_prefill_full_size_sampled(dev):
