@@ -296,3 +296,62 @@ extern "C" bsf_status bsf_route(const int32_t* topk_ids, int64_t T, int64_t kr, 
   }
   return launch_status();
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of bsf_route.
+//
+// For callers that cannot allocate device memory themselves: code running
+// while a CUDA graph is being captured (allocation is not a capturable
+// operation), code inside an allocator-free runtime, or hosts that must not
+// grow device memory after start-up.  The per-chunk expert counts live in a
+// fixed file-scope device array instead of a caller-provided workspace.
+namespace bsf {
+namespace {
+
+constexpr size_t kRouteStaticScratchBytes = BSF_ROUTE_STATIC_SCRATCH_BYTES;
+
+// Shared by every call on a device; every GPU that loads the library holds it until exit.
+static __device__ __align__(256) int32_t g_route_scratch[kRouteStaticScratchBytes / sizeof(int32_t)];
+
+// Device address of g_route_scratch for the current device, resolved once per
+// device with that device current (the host-side name is only a stand-in).
+int32_t* route_scratch_ptr(bsf_status* st) {
+  static int32_t* cached[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *st = BSF_ERR_CUDA;
+    return nullptr;
+  }
+  if (cached[dev] == nullptr) {
+    int32_t* ptr = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_route_scratch) != cudaSuccess || ptr == nullptr) {
+      *st = BSF_ERR_CUDA;
+      return nullptr;
+    }
+    cached[dev] = ptr;
+  }
+  *st = BSF_OK;
+  return cached[dev];
+}
+
+}  // namespace
+}  // namespace bsf
+
+extern "C" bsf_status bsf_route_no_alloc(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout,
+                                         int64_t align_or_max_m, int32_t* counts, int32_t* seg_start,
+                                         int32_t* output_index, int32_t* token_of_row, int32_t* m_indices,
+                                         int64_t m_cap, const uint8_t* q, const int32_t* sf, int64_t sf_ld,
+                                         int64_t K, uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld,
+                                         bsf_stream_t stream) {
+  if (T < 0 || kr <= 0 || E <= 0) return BSF_ERR_INVALID_ARGUMENT;
+  const size_t need = bsf_route_workspace_bytes(T, kr, E);
+  if (need > kRouteStaticScratchBytes) return BSF_ERR_UNSUPPORTED;   // problem larger than the static scratch
+  bsf_status st = BSF_OK;
+  int32_t* scratch = route_scratch_ptr(&st);
+  if (st != BSF_OK) return st;
+  // The count kernel overwrites every scratch word the later kernels read, so
+  // the previous call's contents need no clearing.
+  return bsf_route(topk_ids, T, kr, E, layout, align_or_max_m, counts, seg_start, output_index, token_of_row,
+                   m_indices, m_cap, q, sf, sf_ld, K, a_packed, sfa_packed, sfa_ld, scratch, kRouteStaticScratchBytes,
+                   stream);
+}

@@ -153,6 +153,33 @@ bsf_status bsf_route(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, 
                      size_t workspace_bytes, bsf_stream_t stream);
 
 /*
+ * bsf_route_no_alloc — bsf_route without a caller-provided workspace.
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that cannot allocate device memory at the call site: work recorded while a
+ * CUDA graph is being captured (allocation is not capturable), runtimes that
+ * forbid allocation after start-up, or code without access to an allocator.
+ * Same arguments, outputs and errors as bsf_route minus workspace /
+ * workspace_bytes.  The scratch is a file-scope device array of
+ * BSF_ROUTE_STATIC_SCRATCH_BYTES bytes (256 KiB) that every GPU which loads
+ * the library holds until the process exits; a problem whose
+ * bsf_route_workspace_bytes(T, kr, E) exceeds it is rejected with
+ * BSF_ERR_UNSUPPORTED before anything is enqueued.  The first call on a
+ * device resolves the array's device address (cudaGetSymbolAddress, with that
+ * device current), so make that first call before any stream capture.
+ * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ * All calls on a device share that device's one array, so calls that
+ * overlap on the GPU (for instance on two streams of the same device) race
+ * with each other: order them on one stream.  The array keeps the last call's
+ * contents; every word a call reads is first written by that same call.
+ */
+#define BSF_ROUTE_STATIC_SCRATCH_BYTES (256 * 1024)
+bsf_status bsf_route_no_alloc(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout,
+                              int64_t align_or_max_m, int32_t* counts, int32_t* seg_start, int32_t* output_index,
+                              int32_t* token_of_row, int32_t* m_indices, int64_t m_cap, const uint8_t* q,
+                              const int32_t* sf, int64_t sf_ld, int64_t K, uint8_t* a_packed, int32_t* sfa_packed,
+                              int64_t sfa_ld, bsf_stream_t stream);
+
+/*
  * bsf_grouped_gemm_contig — D[r, :] = BF16( dequant(A[r, :]) . dequant(B_e)^T )
  * for every expert e and every row r in [seg_start[e], seg_start[e] + counts[e]).
  * "GEMM 执行方式" §4.1 (P independent problems), §4.4 (Y_e = X_e W_e^T);
