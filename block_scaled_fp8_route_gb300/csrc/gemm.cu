@@ -39,7 +39,7 @@ constexpr int kBlockK = 128;        // K per pipeline stage (one 128-byte swizzl
 constexpr int kMaxExperts = 1024;
 constexpr int kSfSlots = 4;
 constexpr int kThreads = 320;
-constexpr int kTmaRows = 32;        // token rows per TMA box
+constexpr int kBigTok = 224;        // token tile of the large-segment variant
 
 struct GemmArgs {
   const int32_t* seg_start;  // contiguous: [E+1]; masked: nullptr
@@ -54,11 +54,16 @@ struct GemmArgs {
   int* err;
 };
 
+// TOK = token columns of one accumulator (MMA N <= TOK).  Both variants keep
+// two accumulators in TMEM so the epilogue of one tile overlaps the MMAs of
+// the next: 64: 2 x 64 + 4 x 8 SF columns; 224: 2 x 224 + 4 x 16 = 512.
 template <int TOK>
 struct Cfg {
   static constexpr int kStages = TOK <= 64 ? 8 : 4;
-  static constexpr int kAccBufs = TOK <= 128 ? 2 : 1;
-  static constexpr int kSfCols = TOK <= 64 ? 8 : 16;          // 4 weight-SF columns + TOK/32 token-SF columns
+  static constexpr int kAccBufs = 2;
+  static constexpr int kSfCols = TOK <= 64 ? 8 : 16;          // 4 weight-SF columns + ceil(TOK/32) token-SF columns
+  static constexpr int kTokSfCols = (TOK + 31) / 32;
+  static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK / 2;   // token rows per TMA box (at most 2 boxes per stage)
   static constexpr int kSfBase = kAccBufs * TOK;
   static constexpr int kTmemUsed = kSfBase + kSfSlots * kSfCols;
   static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
@@ -73,6 +78,8 @@ struct Cfg {
   static_assert(kTmemUsed <= 512, "TMEM budget");
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(TOK % 32 == 0 && TOK <= 256, "token tile");
+  static_assert((kBoxRows * kBlockK) % 1024 == 0, "TMA boxes must keep the 1024-byte swizzle alignment");
+  static_assert(4 + kTokSfCols <= kSfCols, "SF slot width");
 };
 
 struct Tile {
@@ -87,14 +94,17 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* tile_start, const 
     if (tile_start[mid] <= t) lo = mid; else hi = mid - 1;
   }
   const int local = t - tile_start[lo];
-  const int nchunks = (cnt[lo] + tok - 1) / tok;
+  const int c = cnt[lo];
+  const int nchunks = (c + tok - 1) / tok;
   const int nt = local / nchunks;
   const int chunk = local - nt * nchunks;
+  // equal chunks (rounded up to 16 rows, never above tok): 264 rows -> 2 x 144
+  const int per = min(tok, ((c + nchunks - 1) / nchunks + 15) & ~15);
   Tile r;
   r.e = lo;
   r.nt = nt;
-  r.tok0 = row0[lo] + chunk * tok;
-  r.ntok = min(tok, cnt[lo] - chunk * tok);
+  r.tok0 = row0[lo] + chunk * per;
+  r.ntok = min(per, c - chunk * per);
   return r;
 }
 
@@ -213,16 +223,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
         const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
-        const int n_loads = (tl.ntok + kTmaRows - 1) / kTmaRows;
-        const uint32_t bytes = C::kStageB + n_loads * kTmaRows * kBlockK;
+        const int n_loads = (tl.ntok + C::kBoxRows - 1) / C::kBoxRows;
+        const uint32_t bytes = C::kStageB + n_loads * C::kBoxRows * kBlockK;
         const int wrow = tl.e * N + tl.nt * kBlockW;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(stage_b + stage * C::kStageB, &tmap_b, &full[stage], kb * kBlockK, wrow);
           for (int i = 0; i < n_loads; ++i)
-            tma_load_2d(stage_a + stage * C::kStageA + i * kTmaRows * kBlockK, &tmap_a, &full[stage], kb * kBlockK,
-                        tl.tok0 + i * kTmaRows);
+            tma_load_2d(stage_a + stage * C::kStageA + i * C::kBoxRows * kBlockK, &tmap_a, &full[stage],
+                        kb * kBlockK, tl.tok0 + i * C::kBoxRows);
           ++issued;
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
@@ -332,9 +342,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) w[c] = static_cast<uint32_t>(__ldg(sfb_base + static_cast<int64_t>(g) * N + 32 * c));
-        uint32_t a[TOK / 32];
+        uint32_t a[C::kTokSfCols + 1];
+        a[C::kTokSfCols] = 0x7F7F7F7Fu;
 #pragma unroll
-        for (int c = 0; c < TOK / 32; ++c) {
+        for (int c = 0; c < C::kTokSfCols; ++c) {
           const int rl = lane + 32 * c;
           const int64_t row = static_cast<int64_t>(tl.tok0) + rl;
           a[c] = (rl < mma_n && row < p.m_rows) ? static_cast<uint32_t>(__ldg(p.sfa + g * p.sfa_ld + row))
@@ -345,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t col = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::kSfBase + sf_slot * C::kSfCols;
         tmem_st_x4(col, w[0], w[1], w[2], w[3]);
 #pragma unroll
-        for (int c = 0; c < TOK / 32; c += 2) tmem_st_x2(col + 4 + c, a[c], a[c + 1]);
+        for (int c = 0; c < C::kTokSfCols; c += 2) tmem_st_x2(col + 4 + c, a[c], a[c + 1]);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -394,7 +405,7 @@ template <int TOK>
 bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int64_t max_tiles, cudaStream_t s) {
   using C = Cfg<TOK>;
   CUtensorMap map_a, map_b;
-  if (!make_map(&map_a, a, args.m_rows, args.K, kTmaRows)) return BSF_ERR_CUDA;
+  if (!make_map(&map_a, a, args.m_rows, args.K, C::kBoxRows)) return BSF_ERR_CUDA;
   if (!make_map(&map_b, b, static_cast<int64_t>(args.E) * args.N, args.K, kBlockW)) return BSF_ERR_CUDA;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -441,8 +452,8 @@ extern "C" bsf_status bsf_grouped_gemm_contig(const uint8_t* a, const int32_t* s
   if (!err) return BSF_ERR_CUDA;
   GemmArgs args{seg_start, counts, 0, m_cap, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
                 static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err};
-  const int64_t max_tiles = (m_cap / 256 + E) * (N / 128);
-  return launch<256>(args, a, b, max_tiles, reinterpret_cast<cudaStream_t>(stream));
+  const int64_t max_tiles = (m_cap / kBigTok + E) * (N / 128);
+  return launch<kBigTok>(args, a, b, max_tiles, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" bsf_status bsf_grouped_gemm_masked(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, const uint8_t* b,
@@ -464,6 +475,6 @@ extern "C" bsf_status bsf_grouped_gemm_masked(const uint8_t* a, const int32_t* s
     const int64_t max_tiles = E * ((max_m + 63) / 64) * (N / 128);
     return launch<64>(args, a, b, max_tiles, s);
   }
-  const int64_t max_tiles = E * ((max_m + 255) / 256) * (N / 128);
-  return launch<256>(args, a, b, max_tiles, s);
+  const int64_t max_tiles = E * ((max_m + kBigTok - 1) / kBigTok) * (N / 128);
+  return launch<kBigTok>(args, a, b, max_tiles, s);
 }
