@@ -209,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) tile_start[E] = carry;
     if (__any_sync(0xffffffffu, bad) && lane == 0 && blockIdx.x == 0) raise_error(p.err, BSF_DEVERR_SEGMENT);
   }
+  __syncwarp();   // warp 0 reconverges after the single-lane set-up before the block barrier
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
