@@ -38,7 +38,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "large", "tiny"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "large", "tiny", "host"])
+    ap.add_argument("--tokens", default="16,32,64,128,256,512,1024,2048,4096",
+                    help="token counts of the host-weight sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -225,10 +227,117 @@ def run_reference(args, w, metric, unit, hib):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- host-weight sweep
+def measure_read_gbs(t, host_mapped, reps=5):
+    """Bandwidth at which the SMs stream-read tensor t (device, or pinned host through its mapped address)."""
+    from block_scaled_fp8_route_gb300 import ops
+    out = torch.empty(1, dtype=torch.int64, device="cuda")
+    for _ in range(2):
+        ops.checksum_u64(t, host_mapped=host_mapped, out=out)
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+        e0.record()
+        ops.checksum_u64(t, host_mapped=host_mapped, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    return t.numel() * t.element_size() / (best / 1e3) / 1e9
+
+
+def run_host_sweep(args, w, metric):
+    """Grouped GEMM with every weight byte in pinned host memory, T swept; one JSON line."""
+    from block_scaled_fp8_route_gb300 import MoEPath, ops, _lib
+    _lib.load()
+    dev = torch.device("cuda", 0)
+    wt = W.weights(w, device=dev)
+    probe = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()        # 1 GiB pinned probe buffer
+    link_gbs = measure_read_gbs(probe, True)
+    h2d_t0 = torch.cuda.Event(True)
+    h2d_t1 = torch.cuda.Event(True)
+    dprobe = torch.empty_like(probe, device=dev)
+    h2d_t0.record()
+    dprobe.copy_(probe, non_blocking=True)
+    h2d_t1.record()
+    torch.cuda.synchronize()
+    memcpy_gbs = probe.numel() / (h2d_t0.elapsed_time(h2d_t1) / 1e3) / 1e9
+    del dprobe
+    sweep = []
+    path = None
+    wq_h = sfb_h = None
+    clocks = ClockSampler(0)
+    clocks.start()
+    for T in [int(v) for v in args.tokens.split(",")]:
+        wT = W.with_tokens(w, T)
+        ids, p = W.routing(wT, device=dev)
+        counts = torch.bincount(ids.flatten().long(), minlength=w.E).cpu().numpy()
+        max_m = W.max_m_for(wT, counts)
+        x = W.activations(wT, device=dev)
+        path = MoEPath(w.E, w.kr, T, w.K, w.N, wt if wq_h is None else wt[:1], layout=W.MASKED,
+                       align_or_max_m=max_m, device=dev, weights_on_host=True, expected_m=T * w.kr // w.E)
+        if wq_h is None:
+            wq_h, sfb_h = path.wq, path.sfb
+        else:
+            path.wq, path.sfb = wq_h, sfb_h
+        for _ in range(args.warmup):
+            path.step(x, ids, p)
+        torch.cuda.synchronize()
+        ev = []
+        orig = path.gemm
+
+        def timed(*a, **k):
+            e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+            e0.record()
+            r = orig(*a, **k)
+            e1.record()
+            ev.append((e0, e1))
+            return r
+
+        path.gemm = timed
+        s0, s1 = torch.cuda.Event(True), torch.cuda.Event(True)
+        s0.record()
+        for _ in range(args.steps):
+            path.step(x, ids, p)
+        s1.record()
+        torch.cuda.synchronize()
+        path.gemm = orig
+        assert ops.device_error() == 0
+        gemm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        active = int((counts > 0).sum())
+        nw = (w.K // 128 + 3) // 4
+        link_bytes = active * (w.N * w.K + w.N * nw * 4)
+        rows = int(np.minimum(counts, max_m).sum())
+        flops = 2.0 * rows * w.N * w.K
+        sweep.append({"T": T, "max_m": max_m, "active_experts": active, "gemm_ms": gemm_ms,
+                      "step_ms": s0.elapsed_time(s1) / args.steps,
+                      "link_gbs": link_bytes / (gemm_ms / 1e3) / 1e9, "tflops": flops / (gemm_ms / 1e3) / 1e12})
+    clk = clocks.stop()
+    last = sweep[-1]
+    line = {
+        "metric": metric, "value": last["link_gbs"], "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": last["step_ms"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 acc -> bf16", "data": "synthetic",
+        "config": {"workload": "host", "T": last["T"], "top_k": w.kr, "experts": w.E, "K": w.K, "N": w.N,
+                   "layout": "masked", "weights": "pinned host memory, read in-kernel through mapped addresses"},
+        "roofline": {"bound": "host-link", "achieved": last["link_gbs"], "peak": link_gbs, "unit": "GB/s",
+                     "frac": last["link_gbs"] / link_gbs, "peak_src": "measured SM stream read of 1 GiB pinned host memory",
+                     "traffic": None, "kernel": "grouped_gemm_kernel"},
+        "host_link": {"sm_read_gbs": link_gbs, "memcpy_h2d_gbs": memcpy_gbs},
+        "sweep": sweep, "clocks": clk, "cpu_baseline": None, "e2e": None,
+        "gpu_launches": 7 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- GPU leg
 def main():
     args = parse()
     w = W.WORKLOADS[args.workload]
+    if args.workload == "host" and args.impl != "reference":
+        run_host_sweep(args, w, "grouped-GEMM TFLOPS & % FP8 roofline (large M); HBM GB/s & % peak (decode)")
+        return
     large_m = w.name in ("prefill", "large")
     metric = "grouped-GEMM TFLOPS & % FP8 roofline (large M); HBM GB/s & % peak (decode)"
     unit = "TFLOP/s" if large_m else "GB/s"

@@ -31,6 +31,7 @@ SIGNATURES = {
     "bsf_grouped_gemm_contig": (_c_int, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p, _i64, _i64, _i64, _c_int, _p]),
     "bsf_grouped_gemm_masked": (_c_int, [_p, _p, _i64, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _c_int, _p]),
     "bsf_combine": (_c_int, [_p, _i64, _p, _p, _i64, _i64, _i64, _p, _p]),
+    "bsf_checksum_u64": (_c_int, [_p, _size, _c_int, _p, _p]),
 }
 
 _LIB = None

@@ -148,6 +148,9 @@ __device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t v0, uint32_t
                "r"(v2), "r"(v3)
                : "memory");
 }
+__device__ __forceinline__ void tmem_st_x1(uint32_t taddr, uint32_t v0) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v0) : "memory");
+}
 __device__ __forceinline__ void tmem_st_x2(uint32_t taddr, uint32_t v0, uint32_t v1) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(v0), "r"(v1) : "memory");
 }

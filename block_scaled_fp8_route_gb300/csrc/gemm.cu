@@ -37,9 +37,9 @@ namespace {
 constexpr int kBlockW = 128;        // weight rows per tile (MMA M)
 constexpr int kBlockK = 128;        // K per pipeline stage (one 128-byte swizzle row of FP8)
 constexpr int kMaxExperts = 1024;
-constexpr int kSfSlots = 4;
 constexpr int kThreads = 320;
 constexpr int kBigTok = 224;        // token tile of the large-segment variant
+constexpr int kHostTok = 448;       // token tile of the host-weight (K-outer / M-inner) variant
 
 struct GemmArgs {
   const int32_t* seg_start;  // contiguous: [E+1]; masked: nullptr
@@ -54,16 +54,26 @@ struct GemmArgs {
   int* err;
 };
 
-// TOK = token columns of one accumulator (MMA N <= TOK).  Both variants keep
-// two accumulators in TMEM so the epilogue of one tile overlaps the MMAs of
-// the next: 64: 2 x 64 + 4 x 8 SF columns; 224: 2 x 224 + 4 x 16 = 512.
+// TOK = token columns of one tile's accumulator.  64 and 224 keep two
+// accumulators in TMEM so the epilogue of one tile overlaps the MMAs of the
+// next (2 x 64 + 4 x 8 SF columns; 2 x 224 + 4 x 16 = 512).  448 holds all
+// tokens of an expert (up to 448) in one accumulator, issued as two MMAs of
+// N <= 224 per K-step, so each weight tile is fetched once and reused for all
+// of them (the K-outer / M-inner order of the "AsymGEMM" README; used when the
+// weights live in host memory and every re-fetch crosses the host link).
 template <int TOK>
 struct Cfg {
-  static constexpr int kStages = TOK <= 64 ? 8 : 4;
-  static constexpr int kAccBufs = 2;
-  static constexpr int kSfCols = TOK <= 64 ? 8 : 16;          // 4 weight-SF columns + ceil(TOK/32) token-SF columns
+  static constexpr int kStages = TOK <= 64 ? 8 : TOK <= 224 ? 4 : 2;
+  static constexpr int kAccBufs = TOK <= 224 ? 2 : 1;
+  static constexpr int kSfSlots = TOK <= 224 ? 4 : 2;
   static constexpr int kTokSfCols = (TOK + 31) / 32;
-  static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK / 2;   // token rows per TMA box (at most 2 boxes per stage)
+  static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK <= 224 ? TOK / 2 : 224;   // token rows per TMA box
+  static constexpr int kSub = TOK <= 224 ? TOK : 224;         // MMA N of one sub-tile (<= 256)
+  // SF slot: 4 weight-SF columns, then per sub-tile kSub/32 token-SF columns
+  // starting every 8 columns (scale-factor TMEM addresses stay 4-column aligned)
+  static constexpr int kSubSfCols = kSub / 32;
+  static constexpr int kSfCols = TOK <= 64 ? 8 : TOK <= 224 ? 16 : 32;
+  static __device__ __forceinline__ int tok_sf_col(int c) { return 4 + (c / kSubSfCols) * 8 + c % kSubSfCols; }
   static constexpr int kSfBase = kAccBufs * TOK;
   static constexpr int kTmemUsed = kSfBase + kSfSlots * kSfCols;
   static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
@@ -75,11 +85,14 @@ struct Cfg {
   static constexpr int kBarBytes = 256;
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kStageB + kStageA) + kEpiBytes +
                                   kTableBytes + kBarBytes;
+  static_assert(kSfBase + kSfSlots * kSfCols <= 512, "TMEM columns");
+  static_assert(4 + (TOK / kSub - 1) * 8 + kSubSfCols <= kSfCols, "SF slot width");
+  static_assert(kSubSfCols <= 8, "token SF columns of a sub-tile");
   static_assert(kTmemUsed <= 512, "TMEM budget");
   static_assert(kSmem <= 232448, "shared memory budget");
-  static_assert(TOK % 32 == 0 && TOK <= 256, "token tile");
+  static_assert(TOK % 32 == 0 && TOK <= 448, "token tile");
+  static_assert(kSub % 32 == 0 && (kSub * kBlockK) % 1024 == 0, "sub-tile alignment");
   static_assert((kBoxRows * kBlockK) % 1024 == 0, "TMA boxes must keep the 1024-byte swizzle alignment");
-  static_assert(4 + kTokSfCols <= kSfCols, "SF slot width");
 };
 
 struct Tile {
@@ -140,8 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = bars;
   uint64_t* empty = full + C::kStages;
   uint64_t* sf_full = empty + C::kStages;
-  uint64_t* sf_empty = sf_full + kSfSlots;
-  uint64_t* acc_full = sf_empty + kSfSlots;
+  uint64_t* sf_empty = sf_full + C::kSfSlots;
+  uint64_t* acc_full = sf_empty + C::kSfSlots;
   uint64_t* acc_empty = acc_full + C::kAccBufs;
   uint64_t* mma_done = acc_empty + C::kAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -159,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < kSfSlots; ++s) {
+    for (int s = 0; s < C::kSfSlots; ++s) {
       mbar_init(&sf_full[s], 4);
       mbar_init(&sf_empty[s], 1);
     }
@@ -265,19 +278,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t sfw = tmem_base + C::kSfBase + sf_slot * C::kSfCols;
           const uint32_t sft = sfw + 4;
-          const uint32_t idesc = idesc_mxf8_e4m3(kBlockW, mma_n, kb & 3, kb & 3);
           const uint64_t adesc = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB));
           const uint64_t bdesc = smem_desc_k_sw128(smem_u32(stage_a + stage * C::kStageA));
+          // sub-tiles of at most kSub tokens: columns j*kSub.., smem rows j*kSub.., token SF columns j*kSub/32..
 #pragma unroll
-          for (int k = 0; k < kBlockK / 32; ++k) {
-            // advance 32 bytes (one K=32 step of FP8) inside the swizzled 128-byte rows
-            mma_mxf8(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sfw, sft, (kb | k) != 0);
+          for (int j = 0; j < TOK / C::kSub; ++j) {
+            const int n_j = static_cast<int>(mma_n) - j * C::kSub;
+            if (n_j <= 0) break;
+            const uint32_t idesc = idesc_mxf8_e4m3(kBlockW, n_j < C::kSub ? n_j : C::kSub, kb & 3, kb & 3);
+            const uint64_t bd = bdesc + static_cast<uint64_t>(j * C::kSub * kBlockK >> 4);
+#pragma unroll
+            for (int k = 0; k < kBlockK / 32; ++k) {
+              // advance 32 bytes (one K=32 step of FP8) inside the swizzled 128-byte rows
+              mma_mxf8(d_tmem + j * C::kSub, adesc + 2 * k, bd + 2 * k, idesc, sfw, sft + j * 8, (kb | k) != 0);
+            }
           }
           tc_commit(&empty[stage]);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
           if ((kb & 3) == 3 || kb == nkb - 1) {
             tc_commit(&sf_empty[sf_slot]);
-            if (++sf_slot == kSfSlots) { sf_slot = 0; sf_phase ^= 1u; }
+            if (++sf_slot == C::kSfSlots) { sf_slot = 0; sf_phase ^= 1u; }
           }
         }
         if (!ok) break;
@@ -343,8 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) w[c] = static_cast<uint32_t>(__ldg(sfb_base + static_cast<int64_t>(g) * N + 32 * c));
-        uint32_t a[C::kTokSfCols + 1];
-        a[C::kTokSfCols] = 0x7F7F7F7Fu;
+        uint32_t a[C::kTokSfCols];
 #pragma unroll
         for (int c = 0; c < C::kTokSfCols; ++c) {
           const int rl = lane + 32 * c;
@@ -357,12 +376,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t col = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::kSfBase + sf_slot * C::kSfCols;
         tmem_st_x4(col, w[0], w[1], w[2], w[3]);
 #pragma unroll
-        for (int c = 0; c < C::kTokSfCols; c += 2) tmem_st_x2(col + 4 + c, a[c], a[c + 1]);
+        for (int c = 0; c < C::kTokSfCols; ++c) tmem_st_x1(col + C::tok_sf_col(c), a[c]);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sf_full[sf_slot]);
-        if (++sf_slot == kSfSlots) { sf_slot = 0; sf_phase ^= 1u; }
+        if (++sf_slot == C::kSfSlots) { sf_slot = 0; sf_phase ^= 1u; }
       }
     }
   }
@@ -424,6 +443,26 @@ bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int6
   return launch_status();
 }
 
+// With BSF_B_HOST_MAPPED, b and sfb are pinned host allocations; the kernel
+// reads them through their device-mapped addresses ("AsymGEMM" README,
+// "Asymmetric Memory Path": weights stay in CPU DRAM and the GPU fetches them
+// in-kernel, no staging copy in HBM).  The pointers must be pinned host
+// allocations (cudaHostAlloc / cudaHostRegister); a pointer the driver cannot
+// map is rejected.
+bsf_status resolve_b(int flags, const uint8_t** b, const int32_t** sfb) {
+  if (!(flags & BSF_B_HOST_MAPPED)) return BSF_OK;
+  void* db = nullptr;
+  void* ds = nullptr;
+  if (cudaHostGetDevicePointer(&db, const_cast<uint8_t*>(*b), 0) != cudaSuccess ||
+      cudaHostGetDevicePointer(&ds, const_cast<int32_t*>(*sfb), 0) != cudaSuccess) {
+    cudaGetLastError();   // clear the sticky-free error of the failed query
+    return BSF_ERR_INVALID_ARGUMENT;
+  }
+  *b = static_cast<const uint8_t*>(db);
+  *sfb = static_cast<const int32_t*>(ds);
+  return BSF_OK;
+}
+
 bsf_status check_common(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, int64_t m_rows, const uint8_t* b,
                         const int32_t* sfb, const void* d, int64_t E, int64_t N, int64_t K, int flags) {
   if (E <= 0 || E > kMaxExperts || N <= 0 || K <= 0 || N % 128 || K % 128) return BSF_ERR_INVALID_ARGUMENT;
@@ -446,15 +485,21 @@ extern "C" bsf_status bsf_grouped_gemm_contig(const uint8_t* a, const int32_t* s
                                               const int32_t* seg_start, const int32_t* counts, int64_t E, int64_t N,
                                               int64_t K, int flags, bsf_stream_t stream) {
   if (m_cap <= 0) return m_cap == 0 ? BSF_OK : BSF_ERR_INVALID_ARGUMENT;
-  const bsf_status st = check_common(a, sfa, sfa_ld, m_cap, b, sfb, d, E, N, K, flags);
+  bsf_status st = check_common(a, sfa, sfa_ld, m_cap, b, sfb, d, E, N, K, flags);
   if (st != BSF_OK) return st;
   if (!seg_start || !counts) return BSF_ERR_INVALID_ARGUMENT;
+  if ((st = resolve_b(flags, &b, &sfb)) != BSF_OK) return st;
   int* err = device_error_ptr();
   if (!err) return BSF_ERR_CUDA;
   GemmArgs args{seg_start, counts, 0, m_cap, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
                 static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (flags & BSF_B_HOST_MAPPED) {   // one tile per (expert, N-tile) up to 448 rows: weights cross the link once
+    const int64_t max_tiles = (m_cap / kHostTok + E) * (N / 128);
+    return launch<kHostTok>(args, a, b, max_tiles, s);
+  }
   const int64_t max_tiles = (m_cap / kBigTok + E) * (N / 128);
-  return launch<kBigTok>(args, a, b, max_tiles, reinterpret_cast<cudaStream_t>(stream));
+  return launch<kBigTok>(args, a, b, max_tiles, s);
 }
 
 extern "C" bsf_status bsf_grouped_gemm_masked(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, const uint8_t* b,
@@ -463,18 +508,26 @@ extern "C" bsf_status bsf_grouped_gemm_masked(const uint8_t* a, const int32_t* s
                                               bsf_stream_t stream) {
   if (max_m <= 0) return BSF_ERR_INVALID_ARGUMENT;
   const int64_t m_rows = E * max_m;
-  const bsf_status st = check_common(a, sfa, sfa_ld, m_rows, b, sfb, d, E, N, K, flags);
+  bsf_status st = check_common(a, sfa, sfa_ld, m_rows, b, sfb, d, E, N, K, flags);
   if (st != BSF_OK) return st;
   if (!masked_m) return BSF_ERR_INVALID_ARGUMENT;
+  if ((st = resolve_b(flags, &b, &sfb)) != BSF_OK) return st;
   int* err = device_error_ptr();
   if (!err) return BSF_ERR_CUDA;
   GemmArgs args{nullptr, masked_m, max_m, m_rows, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
                 static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t hint = expected_m > 0 ? expected_m : max_m;
-  if (max_m <= 64 || hint <= 64) {
+  const bool host = (flags & BSF_B_HOST_MAPPED) != 0;
+  // small slots (or, with weights in HBM, small typical counts): the 64-token variant with its deep ring;
+  // weights in host memory: the smallest variant that holds a whole slot, so weights cross the link once
+  if (max_m <= 64 || (!host && hint <= 32)) {
     const int64_t max_tiles = E * ((max_m + 63) / 64) * (N / 128);
     return launch<64>(args, a, b, max_tiles, s);
+  }
+  if (host && max_m > kBigTok) {
+    const int64_t max_tiles = E * ((max_m + kHostTok - 1) / kHostTok) * (N / 128);
+    return launch<kHostTok>(args, a, b, max_tiles, s);
   }
   const int64_t max_tiles = E * ((max_m + kBigTok - 1) / kBigTok) * (N / 128);
   return launch<kBigTok>(args, a, b, max_tiles, s);

@@ -155,3 +155,13 @@ def combine(y, output_index, topk_weights, z=None, stream=None):
         _ptr(y), rows, _ptr(output_index.contiguous()), _ptr(topk_weights.contiguous()), T, kr, N, _ptr(z),
         _stream(stream)), "combine")
     return z
+
+
+def checksum_u64(t, host_mapped=False, out=None, stream=None):
+    """XOR of the 64-bit words of a tensor's bytes (device tensor, or pinned host tensor if host_mapped)."""
+    nbytes = t.numel() * t.element_size()
+    if out is None:
+        out = torch.empty(1, dtype=torch.int64, device="cuda")
+    _lib.check(_lib.load().bsf_checksum_u64(_ptr(t), nbytes, B_HOST_MAPPED if host_mapped else 0, _ptr(out),
+                                            _stream(stream)), "checksum_u64")
+    return out

@@ -227,6 +227,16 @@ bsf_status bsf_grouped_gemm_masked(const uint8_t* a, const int32_t* sfa, int64_t
 bsf_status bsf_combine(const void* y, int64_t y_rows, const int32_t* output_index, const float* topk_weights,
                        int64_t T, int64_t kr, int64_t N, void* z, bsf_stream_t stream);
 
+/*
+ * bsf_checksum_u64 — streaming read of `bytes` (multiple of 16) at `p`: *out
+ * (device pointer) = XOR of all 64-bit words.  With BSF_B_HOST_MAPPED, `p` is
+ * a pinned host allocation read through its device-mapped address over the
+ * host link.  A measurement and verification helper: it gives the bandwidth
+ * at which the SMs read HBM or host memory (the roofline of the host-weight
+ * mode of the grouped GEMM) and lets tests compare buffer contents.
+ */
+bsf_status bsf_checksum_u64(const void* p, size_t bytes, int flags, unsigned long long* out, bsf_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
