@@ -35,7 +35,7 @@ GEMM_SRC = os.path.join(ROOT, "block_scaled_fp8_route_gb300", "csrc", "gemm.cu")
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "large", "tiny", "host"])
@@ -83,30 +83,91 @@ def step_work(w, counts, placed_rows):
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and throttle reasons sampled every ~2 ms through NVML (ctypes on the
+    driver's libnvidia-ml) while the timed region runs; nvidia-smi as a fallback."""
+
+    # nvmlClocksEventReasons bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.thread = None
+        self.nvml = None
+        self.handle = None
+        self.max_mhz = None
         self.proc = None
         self.lines = []
 
+    def _init_nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        handle = ctypes.c_void_p()
+        uuid = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.gpu).uuid)
+        except Exception:
+            uuid = None
+        ok = False
+        if uuid:
+            u = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            ok = lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(handle)) == 0
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.gpu, ctypes.byref(handle)) != 0:
+            raise OSError("no NVML handle")
+        mx = ctypes.c_uint()
+        lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx))      # NVML_CLOCK_SM
+        self.nvml, self.handle, self.max_mhz = lib, handle, float(mx.value)
+
+    def _loop(self):
+        import ctypes
+        mhz = ctypes.c_uint()
+        reasons = ctypes.c_ulonglong()
+        get_reasons = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop_flag.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0:
+                r = reasons.value if get_reasons(self.handle, ctypes.byref(reasons)) == 0 else 0
+                self.samples.append((float(mhz.value), int(r)))
+            time.sleep(0.002)
+
     def start(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self._init_nvml()
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+            return
+        except (OSError, AttributeError):
+            self.nvml = None
+        try:
+            fields = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                      "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                      "clocks_event_reasons.sw_power_cap")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={fields}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=lambda: [self.lines.append(x.strip()) for x in self.proc.stdout],
+                                           daemon=True)
             self.thread.start()
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def stop(self):
+        if self.nvml is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=2)
+            if not self.samples:
+                return None
+            reasons = set()
+            for _, r in self.samples:
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        reasons.add(name)
+            return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                    "reasons": sorted(reasons), "samples": len(self.samples), "source": "nvml"}
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -114,24 +175,24 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        self.thread.join(timeout=2)
         sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 6:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx = max(mx, float(parts[2]))
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[5:9]):
+            for nm, v in zip(names, parts[2:6]):
                 if v.lower() == "active":
                     reasons.add(nm)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "source": "nvidia-smi"}
 
 
 # ----------------------------------------------------------------------------- traffic record
@@ -156,42 +217,64 @@ def recorded_traffic(workload):
 
 
 # ----------------------------------------------------------------------------- oracle (CPU) leg
-def oracle_sample(w, n_experts, seed=0):
-    """Time the CPU oracle on the path restricted to ``n_experts`` experts (inputs built untimed).
+class OracleSample:
+    """The CPU oracle on the path restricted to ``n_experts`` experts (the busiest ones).
 
-    Returns (seconds, algorithmic bytes, flops, description)."""
-    import oracle
-    rng_t = torch.Generator().manual_seed(seed)
-    wsmall = W.with_tokens(w, w.T)
-    x = W.activations(wsmall)
-    ids, p = W.routing(wsmall)
+    Inputs, including the oracle's quantisation of those experts' weights (a
+    once-per-weight-load step), are prepared untimed; ``run()`` times one pass of
+    quantise -> route -> scatter -> expert GEMMs -> combine and returns
+    (seconds, algorithmic bytes, flops)."""
+
+    def __init__(self, w, n_experts):
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        x = W.activations(w)
+        ids, p = W.routing(w)
+        counts = np.bincount(ids.numpy().reshape(-1), minlength=w.E)
+        self.experts = [int(e) for e in np.argsort(-counts, kind="stable")[:n_experts] if counts[e] > 0]
+        wt = W.weights(w, experts=self.experts)
+        self.xb = x.view(torch.int16).numpy().view(np.uint16)
+        self.ids = ids.numpy()
+        self.p = p.numpy()
+        self.bq, self.bsf = oracle.quantise.quantise_weight(wt.view(torch.int16).numpy().view(np.uint16))
+        self.desc = (f"oracle (float64 numpy) over the {len(self.experts)} busiest of {w.E} experts; quantise, route, "
+                     f"scatter and combine over the whole batch; first GEMM only")
+
+    def run(self):
+        o, w = self.oracle, self.w
+        t0 = time.perf_counter()
+        aq, asf = o.quantise.quantise_act(self.xb)
+        r = o.route.route(self.ids, w.E, w.layout, align=w.align, max_m=w.max_m)
+        a_rows = o.route.scatter_rows(aq, r["token_of_row"])
+        a_sf = o.route.scatter_rows(asf, r["token_of_row"], pad_value=127)
+        y = np.zeros((r["rows_used"], w.N), dtype=np.uint16)
+        rows = 0
+        for i, e in enumerate(self.experts):
+            s, c = int(r["seg_start"][e]), int(r["counts"][e])
+            y[s:s + c] = o.gemm.expert_gemm(a_rows[s:s + c], a_sf[s:s + c], self.bq[i], self.bsf[i])
+            rows += c
+        o.combine.combine(y, r["output_index"], self.p)
+        dt = time.perf_counter() - t0
+        nw = (w.K // 128 + 3) // 4
+        byts = len(self.experts) * (w.N * w.K + w.N * nw * 4) + rows * (w.K + nw * 4 + w.N * 2)
+        return dt, byts, 2.0 * rows * w.N * w.K
+
+
+def workload_config(w):
+    """The ``config`` object of the JSON line (identical for both arms)."""
+    a_or_m = w.max_m if w.layout == W.MASKED else w.align
+    ids, _ = W.routing(w)
     counts = np.bincount(ids.numpy().reshape(-1), minlength=w.E)
-    experts = [int(e) for e in np.argsort(-counts)[:n_experts] if counts[e] > 0]
-    wt = W.weights(w, experts=experts)
-    xb = x.view(torch.int16).numpy().view(np.uint16)
-    wb = wt.view(torch.int16).numpy().view(np.uint16)
-    bq, bsf = oracle.quantise.quantise_weight(wb)          # weights are prepared once, outside the step
-    del rng_t
-    t0 = time.perf_counter()
-    aq, asf = oracle.quantise.quantise_act(xb)
-    r = oracle.route.route(ids.numpy(), w.E, w.layout, align=w.align, max_m=w.max_m)
-    a_rows = oracle.route.scatter_rows(aq, r["token_of_row"])
-    a_sf = oracle.route.scatter_rows(asf, r["token_of_row"], pad_value=127)
-    y = np.zeros((r["rows_used"], w.N), dtype=np.uint16)
-    rows = 0
-    for i, e in enumerate(experts):
-        s, c = int(r["seg_start"][e]), int(r["counts"][e])
-        y[s:s + c] = oracle.gemm.expert_gemm(a_rows[s:s + c], a_sf[s:s + c], bq[i], bsf[i])
-        rows += c
-    oracle.combine.combine(y, r["output_index"], p.numpy())
-    dt = time.perf_counter() - t0
-    K, N = w.K, w.N
-    nw = (K // 128 + 3) // 4
-    byts = len(experts) * (N * K + N * nw * 4) + rows * (K + nw * 4 + N * 2)
-    flops = 2.0 * rows * N * K
-    desc = (f"oracle over {len(experts)} of {w.E} experts ({rows} routed rows; quantise/route/combine over the "
-            f"whole batch), gate-up GEMM only")
-    return dt, byts, flops, desc
+    cfg = {"workload": w.name, "T": w.T, "top_k": w.kr, "experts": w.E, "K": w.K, "N": w.N,
+           "layout": "masked" if w.layout == W.MASKED else "contiguous",
+           "max_m" if w.layout == W.MASKED else "align": a_or_m,
+           "l2": f"no flush: weights {(w.E * w.N * w.K) / 1e9:.2f} GB > 129 MB L2, streamed each step",
+           "routed_rows": int(np.minimum(counts, a_or_m).sum()) if w.layout == W.MASKED else int(counts.sum()),
+           "active_experts": int((counts > 0).sum())}
+    if w.K2:
+        cfg.update({"K2": w.K2, "N2": w.N2})
+    return cfg
 
 
 def host_cores():
@@ -205,22 +288,22 @@ def run_reference(args, w, metric, unit, hib):
     """--impl reference: the oracle as it stands, on the host cores."""
     if int(os.environ.get("RANK", "0")) != 0:
         return
-    n_exp = 8 if w.name == "decode" else 2
+    sample = OracleSample(w, 2 if w.name in ("decode", "host", "tiny") else 1)
     for _ in range(args.warmup):
-        oracle_sample(w, n_exp)
+        sample.run()
     tot_t, tot_b, tot_f = 0.0, 0.0, 0.0
-    desc = ""
     for _ in range(args.steps):
-        dt, b, f, desc = oracle_sample(w, n_exp)
+        dt, b, f = sample.run()
         tot_t += dt
         tot_b += b
         tot_f += f
+    desc = sample.desc
     value = (tot_b / tot_t / 1e9) if unit == "GB/s" else (tot_f / tot_t / 1e12)
     line = {
         "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
         "higher_is_better": hib, "data": "synthetic", "dtype": "f64",
-        "config": {"workload": w.name},
+        "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": unit, "cores": host_cores(), "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -384,7 +467,7 @@ def main():
     for _ in range(args.warmup):
         path.step(x, ids, p, h2)
 
-    # time the GEMM launches with events on the launching stream
+    # eager steps, with CUDA events around every GEMM launch on the launching stream
     gemm_events = []
     orig_gemm = path.gemm
 
@@ -398,9 +481,23 @@ def main():
         return r
 
     path.gemm = timed_gemm
+    torch.cuda.synchronize()
+    q0 = torch.cuda.Event(enable_timing=True)
+    q1 = torch.cuda.Event(enable_timing=True)
+    q0.record(stream)
+    for _ in range(args.steps):
+        path.step(x, ids, p, h2)
+    q1.record(stream)
+    torch.cuda.synchronize()
+    path.gemm = orig_gemm
+    eager_ms = q0.elapsed_time(q1) / args.steps
+
+    # the timed region: the same step replayed from a CUDA graph (launch gaps removed)
+    path.capture(x, ids, p, h2)
+    for _ in range(args.warmup):
+        path.replay()
     clocks = ClockSampler(local)
     clocks.start()
-    time.sleep(0.5)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -408,13 +505,12 @@ def main():
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
-        path.step(x, ids, p, h2)
+        path.replay()
     t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    path.gemm = orig_gemm
     elapsed_ms = t0.elapsed_time(t1)
     if world > 1:
         tt = torch.tensor([elapsed_ms], device=dev)
@@ -456,11 +552,13 @@ def main():
         h2d = hx.numel() * hx.element_size() + hids.numel() * 4 + hp.numel() * 4
         d2h = hz.numel() * hz.element_size()
 
+        path.capture(dx, dids, dp, h2)           # the graph reads the device input buffers
+
         def e2e_step():
             dx.copy_(hx, non_blocking=True)
             dids.copy_(hids, non_blocking=True)
             dp.copy_(hp, non_blocking=True)
-            z = path.step(dx, dids, dp, h2)
+            z = path.replay()
             hz.copy_(z, non_blocking=True)
 
         for _ in range(args.warmup):
@@ -487,20 +585,18 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_exp = 16 if w.name == "decode" else 3
-        dt, b, f, desc = oracle_sample(w, n_exp)
-        cv = (f / dt / 1e12) if large_m else (b / dt / 1e9)
-        cpu = {"value": cv, "unit": unit, "cores": host_cores(), "kind": "oracle", "sample": desc,
-               "seconds": dt}
+        sample = OracleSample(w, 16 if w.name == "decode" else 3)
+        tot_t = tot_b = tot_f = 0.0
+        reps = 0
+        while tot_t < 10.0 and reps < 50:          # about 10 s of oracle time
+            dt, b, f = sample.run()
+            tot_t, tot_b, tot_f, reps = tot_t + dt, tot_b + b, tot_f + f, reps + 1
+        cv = (tot_f / tot_t / 1e12) if large_m else (tot_b / tot_t / 1e9)
+        cpu = {"value": cv, "unit": unit, "cores": host_cores(), "kind": "oracle",
+               "sample": f"{sample.desc}; {reps} passes", "seconds": tot_t}
 
     if rank == 0:
-        cfg = {"workload": w.name, "T": w.T, "top_k": w.kr, "experts": w.E, "K": w.K, "N": w.N,
-               "layout": "masked" if w.layout == W.MASKED else "contiguous",
-               "max_m" if w.layout == W.MASKED else "align": a_or_m,
-               "l2": f"no flush: weights {(w.E * w.N * w.K) / 1e9:.2f} GB > 129 MB L2, streamed each step",
-               "routed_rows": int(counts.sum()), "active_experts": int((counts > 0).sum())}
-        if w.K2:
-            cfg.update({"K2": w.K2, "N2": w.N2})
+        cfg = workload_config(w)
         line = {
             "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
@@ -508,7 +604,8 @@ def main():
             "data": "synthetic", "config": cfg,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
             "gpu_launches": launches_per_step * args.steps,
-            "step_bytes": step_bytes, "step_gemm_flops": flops,
+            "step_bytes": step_bytes, "step_gemm_flops": flops, "eager_ms_per_step": eager_ms,
+            "timed": "CUDA-graph replays of the whole step (eager step time in eager_ms_per_step)",
             "per_kernel_bytes": bytes_by_kernel,
         }
         print(json.dumps(line), flush=True)

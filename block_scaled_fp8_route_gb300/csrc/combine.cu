@@ -38,16 +38,28 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   const bool active = col < N;
-  for (int r = 0; r < kr; ++r) {
-    const int row = __shfl_sync(0xffffffffu, my_row, r);
-    const float p = __shfl_sync(0xffffffffu, my_p, r);
-    if (row < 0 || !active) continue;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + static_cast<int64_t>(row) * N + col));
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  // routes in groups of 8: all loads of a group are issued before any is used
+  for (int r0 = 0; r0 < kr; r0 += 8) {
+    uint4 v[8];
+    float pr[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] = fmaf(p, __uint_as_float(w[i] << 16), acc[2 * i]);
-      acc[2 * i + 1] = fmaf(p, __uint_as_float(w[i] & 0xFFFF0000u), acc[2 * i + 1]);
+    for (int j = 0; j < 8; ++j) {
+      const int row = __shfl_sync(0xffffffffu, my_row, (r0 + j) & 31);
+      pr[j] = __shfl_sync(0xffffffffu, my_p, (r0 + j) & 31);
+      const bool use = active && r0 + j < kr && row >= 0;
+      v[j] = use ? __ldg(reinterpret_cast<const uint4*>(y + static_cast<int64_t>(row) * N + col))
+                 : make_uint4(0, 0, 0, 0);
+      if (!use) pr[j] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (r0 + j >= kr) break;
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(pr[j], __uint_as_float(w[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(pr[j], __uint_as_float(w[i] & 0xFFFF0000u), acc[2 * i + 1]);
+      }
     }
   }
   if (!active) return;

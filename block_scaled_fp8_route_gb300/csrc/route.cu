@@ -11,6 +11,7 @@
 // Unlike an atomic scatter (whose order inside an expert is arbitrary, §4.6),
 // ranks here are stable in the flat assignment index t * k_r + r, so every
 // output is bit-reproducible:
+//   route_small   count + scan + ranks in one CTA for small batches (decode)
 //   route_count   per-chunk expert histograms          (grid: chunks of 2048 assignments)
 //   route_scan    per-expert prefix over chunks, M_e, aligned segment starts (1 CTA)
 //   route_assign  stable ranks -> output_index, token_of_row (grid: chunks)
@@ -178,10 +179,117 @@ __global__ void __launch_bounds__(kThreads) route_assign_kernel(const int32_t* _
   if (threadIdx.x == 0 && overflow) raise_error(err, BSF_DEVERR_SEGMENT);
 }
 
+// Small batches (decode): one CTA of 1024 threads does count, scan and stable
+// ranks in one launch (the single-block routing of "CuTeDSL bei Perplexity"'s
+// decode dispatch), in rounds of 1024 assignments.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallWarps = kSmallThreads / 32;
+constexpr int kSmallMaxE = 256;
+constexpr int64_t kSmallMaxR = 16384;
+
+__global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const int32_t* __restrict__ ids, int64_t R,
+                                                                    int kr, int E, int layout, int64_t a_or_m,
+                                                                    int64_t m_cap, int32_t* __restrict__ counts,
+                                                                    int32_t* __restrict__ seg_start,
+                                                                    int32_t* __restrict__ output_index,
+                                                                    int32_t* __restrict__ token_of_row, int* err) {
+  __shared__ int hist[kSmallMaxE];
+  __shared__ int base[kSmallMaxE];
+  __shared__ int seg[kSmallMaxE];
+  __shared__ int warp_cnt[kSmallWarps][kSmallMaxE];
+  __shared__ int warp_sums[kSmallWarps];
+  __shared__ int flags;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid < E) hist[tid] = 0;
+  if (tid == 0) flags = 0;
+  __syncthreads();
+  for (int64_t i = tid; i < R; i += kSmallThreads) {
+    const int id = ids[i];
+    if (id >= E) atomicOr(&flags, BSF_DEVERR_EXPERT_ID);
+    else if (id >= 0) atomicAdd(&hist[id], 1);
+  }
+  __syncthreads();
+  // segments: masked slots, or an exclusive scan of the aligned lengths (E <= 256: 8 warps)
+  const int M = tid < E ? hist[tid] : 0;
+  if (layout == BSF_LAYOUT_MASKED) {
+    if (tid < E) {
+      const int placed = M < a_or_m ? M : static_cast<int>(a_or_m);
+      counts[tid] = placed;
+      seg[tid] = static_cast<int>(tid * a_or_m);
+      seg_start[tid] = seg[tid];
+      if (M > a_or_m) atomicOr(&flags, BSF_DEVERR_MASKED_OVERFLOW);
+    }
+    if (tid == 0) seg_start[E] = static_cast<int32_t>(E * a_or_m);
+  } else {
+    const int len = tid < E ? static_cast<int>((M + a_or_m - 1) / a_or_m * a_or_m) : 0;
+    int incl = len;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    int prefix = 0;
+    for (int w = 0; w < warp; ++w) prefix += warp_sums[w];
+    if (tid < E) {
+      seg[tid] = prefix + incl - len;
+      counts[tid] = M;
+      seg_start[tid] = seg[tid];
+      if (tid == E - 1) {
+        seg_start[E] = prefix + incl;
+        if (prefix + incl > m_cap) atomicOr(&flags, BSF_DEVERR_SEGMENT);
+      }
+    }
+  }
+  if (tid < E) base[tid] = 0;
+  __syncthreads();
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int64_t r0 = 0; r0 < R; r0 += kSmallThreads) {
+    for (int j = tid; j < kSmallWarps * kSmallMaxE; j += kSmallThreads) (&warp_cnt[0][0])[j] = 0;
+    __syncthreads();
+    const int64_t i = r0 + tid;
+    const int id = i < R ? ids[i] : -1;
+    const bool valid = id >= 0 && id < E;
+    const uint32_t peers = __match_any_sync(0xffffffffu, valid ? id : -1);
+    if (valid && (peers & lt_mask) == 0) warp_cnt[warp][id] = __popc(peers);
+    __syncthreads();
+    if (tid < E) {      // warp-order exclusive prefix on top of the running base
+      int run = base[tid];
+      for (int w = 0; w < kSmallWarps; ++w) {
+        const int c = warp_cnt[w][tid];
+        warp_cnt[w][tid] = run;
+        run += c;
+      }
+      base[tid] = run;
+    }
+    __syncthreads();
+    if (i < R) {
+      int64_t dest = -1;
+      if (valid) {
+        const int rank = warp_cnt[warp][id] + __popc(peers & lt_mask);
+        if (layout == BSF_LAYOUT_MASKED) {
+          if (rank < a_or_m) dest = static_cast<int64_t>(id) * a_or_m + rank;
+        } else {
+          dest = static_cast<int64_t>(seg[id]) + rank;
+        }
+        if (dest >= m_cap) {
+          dest = -1;
+          atomicOr(&flags, BSF_DEVERR_SEGMENT);
+        }
+      }
+      output_index[i] = static_cast<int32_t>(dest);
+      if (dest >= 0) token_of_row[dest] = static_cast<int32_t>(i / kr);
+    }
+    __syncthreads();
+  }
+  if (tid == 0 && flags) raise_error(err, flags);
+}
+
 constexpr int kFillRows = 32;   // packed rows per CTA in route_fill
 
 // Per packed row r < seg_start[E]: mark padding rows (token -1), write
-// m_indices, copy the token's FP8 row and SF words (zeros / bytes 127 for padding).
+// m_indices, and copy a routed row's FP8 data and SF words.
 __global__ void __launch_bounds__(kThreads) route_fill_kernel(int E, int64_t m_cap, const int32_t* __restrict__ counts,
                                                               const int32_t* __restrict__ seg_start,
                                                               int32_t* __restrict__ token_of_row,
@@ -217,29 +325,26 @@ __global__ void __launch_bounds__(kThreads) route_fill_kernel(int E, int64_t m_c
   }
   __syncthreads();
   if (q == nullptr) return;
-  // SF words: thread (word i, row) with consecutive rows -> coalesced stores
+  // SF words of routed rows: thread (word i, row) with consecutive rows -> coalesced stores.
+  // Padding rows keep whatever the buffer held: "GEMM 执行方式" §4.6 leaves them
+  // uninitialised, and no computed output row depends on them.
   const int64_t n_words = (K + 511) / 512;
   for (int64_t j = threadIdx.x; j < n_words * kFillRows; j += kThreads) {
     const int64_t i = j / kFillRows;
     const int rl = static_cast<int>(j % kFillRows);
     const int t = tok[rl];
-    if (t == -2) continue;
-    sfa_packed[i * sfa_ld + row0 + rl] = t >= 0 ? sf[i * sf_ld + t] : 0x7F7F7F7F;
+    if (t < 0) continue;
+    sfa_packed[i * sfa_ld + row0 + rl] = sf[i * sf_ld + t];
   }
-  // FP8 rows: one warp per row, 16-byte vectors
+  // FP8 rows: one warp per routed row, 16-byte vectors
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nvec = K / 16;
   for (int rl = warp; rl < kFillRows; rl += kWarps) {
     const int t = tok[rl];
-    if (t == -2) continue;
+    if (t < 0) continue;
     uint4* dst = reinterpret_cast<uint4*>(a_packed + (row0 + rl) * K);
-    if (t >= 0) {
-      const uint4* src = reinterpret_cast<const uint4*>(q + static_cast<int64_t>(t) * K);
-      for (int64_t v = lane; v < nvec; v += 32) dst[v] = __ldg(src + v);
-    } else {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      for (int64_t v = lane; v < nvec; v += 32) dst[v] = z;
-    }
+    const uint4* src = reinterpret_cast<const uint4*>(q + static_cast<int64_t>(t) * K);
+    for (int64_t v = lane; v < nvec; v += 32) dst[v] = __ldg(src + v);
   }
 }
 
@@ -280,14 +385,20 @@ extern "C" bsf_status bsf_route(const int32_t* topk_ids, int64_t T, int64_t kr, 
   const int nblk = static_cast<int>((R + kChunk - 1) / kChunk);
   int32_t* blk = static_cast<int32_t*>(workspace);
   const int e32 = static_cast<int>(E);
-  if (nblk > 0) {
-    route_count_kernel<<<nblk, kThreads, 0, s>>>(topk_ids, R, e32, blk, err);
-  }
-  route_scan_kernel<<<1, 1024, 0, s>>>(blk, nblk, e32, layout, align_or_max_m, m_cap, counts, seg_start, err);
-  if (nblk > 0) {
-    const size_t smem = static_cast<size_t>(kWarps + 1) * E * sizeof(int);
-    route_assign_kernel<<<nblk, kThreads, smem, s>>>(topk_ids, R, static_cast<int>(kr), e32, layout, align_or_max_m,
-                                                     m_cap, blk, seg_start, output_index, token_of_row, err);
+  if (R <= kSmallMaxR && E <= kSmallMaxE) {
+    route_small_kernel<<<1, kSmallThreads, 0, s>>>(topk_ids, R, static_cast<int>(kr), e32, layout, align_or_max_m,
+                                                   m_cap, counts, seg_start, output_index, token_of_row, err);
+  } else {
+    if (nblk > 0) {
+      route_count_kernel<<<nblk, kThreads, 0, s>>>(topk_ids, R, e32, blk, err);
+    }
+    route_scan_kernel<<<1, 1024, 0, s>>>(blk, nblk, e32, layout, align_or_max_m, m_cap, counts, seg_start, err);
+    if (nblk > 0) {
+      const size_t smem = static_cast<size_t>(kWarps + 1) * E * sizeof(int);
+      route_assign_kernel<<<nblk, kThreads, smem, s>>>(topk_ids, R, static_cast<int>(kr), e32, layout,
+                                                       align_or_max_m, m_cap, blk, seg_start, output_index,
+                                                       token_of_row, err);
+    }
   }
   const int64_t fill_blocks = (m_cap + kFillRows - 1) / kFillRows;
   if (fill_blocks > 0) {

@@ -65,3 +65,24 @@ class MoEPath:
             out = self.y2
         ops.combine(out, self.bufs.output_index, topk_weights, z=self.z)
         return self.z
+
+    def capture(self, x, topk_ids, topk_weights, h2=None):
+        """Record one step on these (static) input tensors into a CUDA graph.
+
+        Every library call is stream-ordered with no host synchronisation or
+        allocation, so the whole step is capturable; a first eager step runs
+        before the capture so that one-time set-up (symbol lookups, kernel
+        attributes) happens outside it.  ``replay()`` re-runs the step on
+        whatever the input tensors hold.
+        """
+        self.step(x, topk_ids, topk_weights, h2)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.step(x, topk_ids, topk_weights, h2)
+        self.graph = graph
+        return graph
+
+    def replay(self):
+        self.graph.replay()
+        return self.z

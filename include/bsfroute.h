@@ -138,9 +138,10 @@ bsf_status bsf_prepare_weight_sf(const float* sf128, int64_t E, int64_t N, int64
  *   q, sf, sf_ld  optional scatter source (NULL: indices only): e4m3 [T, K]
  *                 and packed SF [ceil(K/512)][sf_ld] from bsf_quantise_act.
  *   a_packed      e4m3 [m_cap, K] (output): row r = q[token_of_row[r]];
- *                 padding rows are zero.
+ *                 padding rows are not written (uninitialised, as in §4.6;
+ *                 no GEMM output row that is stored depends on them).
  *   sfa_packed    int32 [ceil(K/512)][sfa_ld] (output), sfa_ld >= m_cap,
- *                 multiple of 4; padding rows get bytes 127.
+ *                 multiple of 4; padding rows are not written.
  *   workspace     device scratch of bsf_route_workspace_bytes(T, kr, E) bytes.
  * Order inside an expert: ascending flat index t*kr + r (stable; the order of
  * the worked example in §4.3 / §4.6).  Deterministic.

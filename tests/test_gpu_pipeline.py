@@ -83,3 +83,24 @@ def test_end_to_end_deterministic(dev):
     first = path.step(xs, idss, ps).clone()
     for _ in range(19):
         assert torch.equal(path.step(xs, idss, ps).view(torch.int16), first.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["decode", "tiny_a128"])
+def test_graph_replay_matches_eager_step(dev, name):
+    w = W.WORKLOADS[name]
+    x, wt = W.activations(w).to(dev), W.weights(w)
+    ids, p = W.routing(w)
+    ids, p = ids.to(dev), p.to(dev)
+    a_or_m = w.max_m if w.layout == W.MASKED else w.align
+    path = MoEPath(w.E, w.kr, w.T, w.K, w.N, wt, layout=w.layout, align_or_max_m=a_or_m, device=dev)
+    eager = path.step(x, ids, p).clone()
+    path.capture(x, ids, p)
+    for _ in range(3):
+        assert torch.equal(path.replay().view(torch.int16), eager.view(torch.int16))
+    # new inputs written into the captured buffers are picked up by the replay
+    x2 = W.activations(W.Workload(**{**w.__dict__, "seed": w.seed + 1})).to(dev)
+    x.copy_(x2)
+    expect = MoEPath(w.E, w.kr, w.T, w.K, w.N, wt, layout=w.layout, align_or_max_m=a_or_m,
+                     device=dev).step(x2, ids, p)
+    assert torch.equal(path.replay().view(torch.int16), expect.view(torch.int16))
+    assert ops.device_error() == 0
