@@ -61,11 +61,15 @@ struct GemmArgs {
 // N <= 224 per K-step, so each weight tile is fetched once and reused for all
 // of them (the K-outer / M-inner order of the "AsymGEMM" README; used when the
 // weights live in host memory and every re-fetch crosses the host link).
-template <int TOK>
+// CPS = CTAs resident per SM.  With CPS = 2 each CTA keeps one accumulator
+// and half the ring, and the two CTAs' single-thread MMA issuers share the
+// SM's tensor core, so one CTA's barrier waits and epilogue drain are covered
+// by the other's MMAs.
+template <int TOK, int CPS = 1>
 struct Cfg {
-  static constexpr int kStages = TOK <= 64 ? 8 : TOK <= 224 ? 4 : 2;
-  static constexpr int kAccBufs = TOK <= 224 ? 2 : 1;
-  static constexpr int kSfSlots = TOK <= 224 ? 4 : 2;
+  static constexpr int kStages = CPS == 2 ? (TOK <= 64 ? 3 : 2) : TOK <= 64 ? 8 : TOK <= 224 ? 4 : 2;
+  static constexpr int kAccBufs = (CPS == 1 && TOK <= 224) ? 2 : 1;
+  static constexpr int kSfSlots = (CPS == 1 && TOK <= 224) ? 4 : 2;
   static constexpr int kTokSfCols = (TOK + 31) / 32;
   static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK <= 224 ? TOK / 2 : 224;   // token rows per TMA box
   static constexpr int kSub = TOK <= 224 ? TOK : 224;         // MMA N of one sub-tile (<= 256)
@@ -89,7 +93,8 @@ struct Cfg {
   static_assert(4 + (TOK / kSub - 1) * 8 + kSubSfCols <= kSfCols, "SF slot width");
   static_assert(kSubSfCols <= 8, "token SF columns of a sub-tile");
   static_assert(kTmemUsed <= 512, "TMEM budget");
-  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kSmem * CPS + 1024 * CPS <= 233472, "shared memory budget");
+  static_assert(kTmemCols * CPS <= 512, "TMEM budget of the CTAs on one SM");
   static_assert(TOK % 32 == 0 && TOK <= 448, "token tile");
   static_assert(kSub % 32 == 0 && (kSub * kBlockK) % 1024 == 0, "sub-tile alignment");
   static_assert((kBoxRows * kBlockK) % 1024 == 0, "TMA boxes must keep the 1024-byte swizzle alignment");
@@ -136,11 +141,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int TOK>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int TOK, int CPS>
+__global__ void __launch_bounds__(kThreads, CPS)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_a,
                         const GemmArgs p) {
-  using C = Cfg<TOK>;
+  using C = Cfg<TOK, CPS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_b = smem;
@@ -421,9 +426,9 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int TOK>
+template <int TOK, int CPS = 1>
 bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int64_t max_tiles, cudaStream_t s) {
-  using C = Cfg<TOK>;
+  using C = Cfg<TOK, CPS>;
   CUtensorMap map_a, map_b;
   if (!make_map(&map_a, a, args.m_rows, args.K, C::kBoxRows)) return BSF_ERR_CUDA;
   if (!make_map(&map_b, b, static_cast<int64_t>(args.E) * args.N, args.K, kBlockW)) return BSF_ERR_CUDA;
@@ -431,15 +436,19 @@ bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int6
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<TOK, CPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::kSmem)) != cudaSuccess)
+      return BSF_ERR_CUDA;
+    if (CPS > 1 && cudaFuncSetAttribute(grouped_gemm_kernel<TOK, CPS>,
+                                        cudaFuncAttributePreferredSharedMemoryCarveout,
+                                        cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return BSF_ERR_CUDA;
     attr_set[dev] = true;
   }
-  int64_t grid = sm_count();
+  int64_t grid = static_cast<int64_t>(sm_count()) * CPS;
   if (max_tiles < grid) grid = max_tiles;
   if (grid <= 0) return BSF_OK;
-  grouped_gemm_kernel<TOK><<<static_cast<unsigned>(grid), kThreads, C::kSmem, s>>>(map_b, map_a, args);
+  grouped_gemm_kernel<TOK, CPS><<<static_cast<unsigned>(grid), kThreads, C::kSmem, s>>>(map_b, map_a, args);
   return launch_status();
 }
 
@@ -499,7 +508,7 @@ extern "C" bsf_status bsf_grouped_gemm_contig(const uint8_t* a, const int32_t* s
     return launch<kHostTok>(args, a, b, max_tiles, s);
   }
   const int64_t max_tiles = (m_cap / kBigTok + E) * (N / 128);
-  return launch<kBigTok>(args, a, b, max_tiles, s);
+  return launch<kBigTok, 2>(args, a, b, max_tiles, s);
 }
 
 extern "C" bsf_status bsf_grouped_gemm_masked(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, const uint8_t* b,
@@ -523,12 +532,12 @@ extern "C" bsf_status bsf_grouped_gemm_masked(const uint8_t* a, const int32_t* s
   // weights in host memory: the smallest variant that holds a whole slot, so weights cross the link once
   if (max_m <= 64 || (!host && hint <= 32)) {
     const int64_t max_tiles = E * ((max_m + 63) / 64) * (N / 128);
-    return launch<64>(args, a, b, max_tiles, s);
+    return launch<64, 2>(args, a, b, max_tiles, s);
   }
   if (host && max_m > kBigTok) {
     const int64_t max_tiles = E * ((max_m + kHostTok - 1) / kHostTok) * (N / 128);
     return launch<kHostTok>(args, a, b, max_tiles, s);
   }
   const int64_t max_tiles = E * ((max_m + kBigTok - 1) / kBigTok) * (N / 128);
-  return launch<kBigTok>(args, a, b, max_tiles, s);
+  return launch<kBigTok, 2>(args, a, b, max_tiles, s);
 }
