@@ -71,7 +71,7 @@ struct Cfg {
   static constexpr int kAccBufs = (CPS == 1 && TOK <= 224) ? 2 : 1;
   static constexpr int kSfSlots = (CPS == 1 && TOK <= 224) ? 4 : 2;
   static constexpr int kTokSfCols = (TOK + 31) / 32;
-  static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK <= 224 ? TOK / 2 : 224;   // token rows per TMA box
+  static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK <= 224 ? 56 : 224;   // token rows per TMA box
   static constexpr int kSub = TOK <= 224 ? TOK : 224;         // MMA N of one sub-tile (<= 256)
   // SF slot: 4 weight-SF columns, then per sub-tile kSub/32 token-SF columns
   // starting every 8 columns (scale-factor TMEM addresses stay 4-column aligned)
@@ -96,6 +96,7 @@ struct Cfg {
   static_assert(kSmem * CPS + 1024 * CPS <= 233472, "shared memory budget");
   static_assert(kTmemCols * CPS <= 512, "TMEM budget of the CTAs on one SM");
   static_assert(TOK % 32 == 0 && TOK <= 448, "token tile");
+  static_assert(TOK % kBoxRows == 0, "whole TMA boxes must fit the token stage");
   static_assert(kSub % 32 == 0 && (kSub * kBlockK) % 1024 == 0, "sub-tile alignment");
   static_assert((kBoxRows * kBlockK) % 1024 == 0, "TMA boxes must keep the 1024-byte swizzle alignment");
 };
