@@ -52,6 +52,7 @@ struct GemmArgs {
   uint16_t* d;
   int E, N, K;
   int* err;
+  int withhold_loads;        // test-only fault injection (BSF_DEBUG_WITHHOLD_LOADS)
 };
 
 // TOK = token columns of one tile's accumulator.  64 and 224 keep two
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       int issued = 0;
-      bool ok = true;
+      bool ok = !p.withhold_loads;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
         const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
         const int n_loads = (tl.ntok + C::kBoxRows - 1) / C::kBoxRows;
@@ -476,7 +477,7 @@ bsf_status resolve_b(int flags, const uint8_t** b, const int32_t** sfb) {
 bsf_status check_common(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, int64_t m_rows, const uint8_t* b,
                         const int32_t* sfb, const void* d, int64_t E, int64_t N, int64_t K, int flags) {
   if (E <= 0 || E > kMaxExperts || N <= 0 || K <= 0 || N % 128 || K % 128) return BSF_ERR_INVALID_ARGUMENT;
-  if (flags & ~BSF_B_HOST_MAPPED) return BSF_ERR_INVALID_ARGUMENT;
+  if (flags & ~(BSF_B_HOST_MAPPED | BSF_DEBUG_WITHHOLD_LOADS)) return BSF_ERR_INVALID_ARGUMENT;
   if (!a || !sfa || !b || !sfb || !d) return BSF_ERR_INVALID_ARGUMENT;
   if (sfa_ld < m_rows || sfa_ld % 4) return BSF_ERR_INVALID_ARGUMENT;
   if (!aligned16(a) || !aligned16(b) || !aligned16(d) || !aligned16(sfa) || !aligned16(sfb))
@@ -502,7 +503,8 @@ extern "C" bsf_status bsf_grouped_gemm_contig(const uint8_t* a, const int32_t* s
   int* err = device_error_ptr();
   if (!err) return BSF_ERR_CUDA;
   GemmArgs args{seg_start, counts, 0, m_cap, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
-                static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err};
+                static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
+                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (flags & BSF_B_HOST_MAPPED) {   // one tile per (expert, N-tile) up to 448 rows: weights cross the link once
     const int64_t max_tiles = (m_cap / kHostTok + E) * (N / 128);
@@ -525,7 +527,8 @@ extern "C" bsf_status bsf_grouped_gemm_masked(const uint8_t* a, const int32_t* s
   int* err = device_error_ptr();
   if (!err) return BSF_ERR_CUDA;
   GemmArgs args{nullptr, masked_m, max_m, m_rows, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
-                static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err};
+                static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
+                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t hint = expected_m > 0 ? expected_m : max_m;
   const bool host = (flags & BSF_B_HOST_MAPPED) != 0;

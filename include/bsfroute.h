@@ -61,6 +61,11 @@ typedef enum bsf_status {
 
 /* GEMM flags. */
 #define BSF_B_HOST_MAPPED 0x1 /* b / sfb are host pointers to pinned, mapped host memory */
+/* Fault injection for tests of the failure path: the kernel's load producer
+ * withholds every load, so each consumer's bounded wait runs out; the kernel
+ * sets BSF_DEVERR_TIMEOUT, releases its tensor memory and returns without
+ * writing d.  No GPU fault or hang is involved. */
+#define BSF_DEBUG_WITHHOLD_LOADS 0x100
 
 const char* bsf_status_string(bsf_status status);
 int bsf_version(void);
