@@ -1,0 +1,93 @@
+"""The pins catch plausible mistakes: each test plants one mistake in the oracle
+(on the CPU, through monkeypatching) and checks that the corresponding pin
+test fails.  Nothing here touches a GPU."""
+
+import numpy as np
+import pytest
+
+from oracle import combine, formats, gemm, quantise, route
+from tests import test_oracle_combine as pin_combine
+from tests import test_oracle_formats as pin_formats
+from tests import test_oracle_gemm as pin_gemm
+from tests import test_oracle_quantise as pin_quantise
+from tests import test_oracle_route as pin_route
+
+
+def _fails(fn, *args):
+    with pytest.raises(AssertionError):
+        fn(*args)
+
+
+def test_ties_away_from_zero_is_caught(monkeypatch):
+    orig = formats.e4m3_encode
+
+    def ties_up(x):
+        x = np.asarray(x, dtype=np.float64)
+        return orig(np.nextafter(np.abs(x), np.inf) * np.sign(x) + 0.0 * x)   # nudges ties upwards
+
+    monkeypatch.setattr(formats, "e4m3_encode", ties_up)
+    _fails(pin_formats.test_e4m3_encode_ties_to_even)
+
+
+def test_double_rounding_bf16_is_caught(monkeypatch):
+    def via_float32(x):
+        x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
+        b = x32.view(np.uint32).astype(np.uint64)
+        r = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+        return r
+
+    monkeypatch.setattr(formats, "bf16_round", via_float32)
+    _fails(pin_formats.test_bf16_round_is_a_single_rounding)
+
+
+def test_floor_instead_of_ceil_exponent_is_caught(monkeypatch):
+    orig = quantise._block_exponent
+    monkeypatch.setattr(quantise, "_block_exponent", lambda amax: orig(amax) - 1)
+    _fails(pin_quantise.test_block_exponent_is_least_with_amax_bound)
+
+
+def test_reversed_order_inside_expert_is_caught(monkeypatch, golden_dir):
+    orig = np.argsort
+
+    def unstable(a, kind=None, **kw):
+        idx = orig(a, kind="stable", **kw)
+        return idx[::-1][orig(np.asarray(a)[idx[::-1]], kind="stable")]   # same keys, reversed ties
+
+    monkeypatch.setattr(route.np, "argsort", unstable)
+    import json
+    import os
+    with open(os.path.join(golden_dir, "routing_example_t5_kr2_e4.json")) as f:
+        ex = json.load(f)
+    _fails(pin_route.test_worked_example_unaligned, ex)
+
+
+def test_wrong_scale_block_index_is_caught(monkeypatch):
+    def shifted(q, sf_bytes):
+        v = formats.e4m3_decode(q)
+        s = formats.ue8m0_to_scale(np.roll(sf_bytes, 1, axis=1))
+        return v * np.repeat(s, quantise.BLOCK, axis=1)
+
+    monkeypatch.setattr(gemm, "dequant_rows", shifted)
+    _fails(pin_gemm.test_exact_rational_brute_force)
+
+
+def test_wrong_weight_rows_are_caught(monkeypatch):
+    orig = gemm.expert_gemm
+
+    def reversed_rows(a_q, a_sf, b_q_e, b_sf_e):
+        return orig(a_q, a_sf, b_q_e[::-1].copy(), b_sf_e[::-1].copy())   # output column n uses weight row N-1-n
+
+    monkeypatch.setattr(gemm, "expert_gemm", reversed_rows)
+
+    monkeypatch.setattr(gemm, "expert_gemm", neighbour_expert)
+    _fails(pin_gemm.test_exact_rational_brute_force)
+
+
+def test_dropped_routing_weight_is_caught(monkeypatch, golden_dir):
+    orig = combine.combine
+
+    def unweighted(y_bits, output_index, topk_weights):
+        return orig(y_bits, output_index, np.ones_like(np.asarray(topk_weights)))
+
+    monkeypatch.setattr(combine, "combine", unweighted)
+    _fails(pin_combine.test_page_formula_z0, golden_dir)
