@@ -78,8 +78,6 @@ def test_wrong_weight_rows_are_caught(monkeypatch):
         return orig(a_q, a_sf, b_q_e[::-1].copy(), b_sf_e[::-1].copy())   # output column n uses weight row N-1-n
 
     monkeypatch.setattr(gemm, "expert_gemm", reversed_rows)
-
-    monkeypatch.setattr(gemm, "expert_gemm", neighbour_expert)
     _fails(pin_gemm.test_exact_rational_brute_force)
 
 
