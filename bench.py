@@ -43,6 +43,8 @@ def parse():
                     help="token counts of the host-weight sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-large-m", action="store_true",
+                    help="skip the large-M GEMM measurements added to the decode line")
     return ap.parse_args()
 
 
@@ -414,6 +416,69 @@ def run_host_sweep(args, w, metric):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- large-M GEMMs (context object)
+def large_m_gemms(dev, pk, reps=10):
+    """Gate-up and down grouped GEMMs of the prefill and large workloads, timed
+    alone (CUDA events on the launch stream), plus a library FP8 GEMM for context."""
+    from block_scaled_fp8_route_gb300 import ops
+    out = {}
+    fp8_peak = 2.0 * pk["bf16_tflops"]
+    for name in ("prefill", "large"):
+        w = W.WORKLOADS[name]
+        ids, _ = W.routing(w, device=dev)
+        bufs = ops.route(ids, w.E, w.layout, w.align)
+        rows = int(bufs.counts.sum().item())
+        res = {}
+        for tag, (K, N) in enumerate(((w.K, w.N), (w.K2, w.N2))):
+            x = W.activations(W.with_tokens(w, bufs.m_cap), device=dev, K=K, tag=tag)
+            aq, asf = ops.quantise_act(x)
+            del x
+            wt = W.weights(w, device=dev, N=N, K=K, tag=tag)
+            bq, sf128 = ops.quantise_weight(wt)
+            del wt
+            sfb = ops.prepare_weight_sf(sf128, K)
+            d = torch.empty((bufs.m_cap, N), dtype=torch.bfloat16, device=dev)
+            for _ in range(3):
+                ops.grouped_gemm_contig(aq, asf, bq, sfb, bufs.seg_start, bufs.counts, d=d)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+            e0.record()
+            for _ in range(reps):
+                ops.grouped_gemm_contig(aq, asf, bq, sfb, bufs.seg_start, bufs.counts, d=d)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            tf = 2.0 * rows * N * K / (ms / 1e3) / 1e12
+            res["gate_up" if tag == 0 else "down"] = {"K": K, "N": N, "ms": ms, "tflops": tf, "frac": tf / fp8_peak}
+            del aq, asf, bq, sf128, sfb, d
+            torch.cuda.empty_cache()
+        out[name] = {"routed_rows": rows, **res}
+    out["fp8_peak_tflops"] = fp8_peak
+    out["fp8_peak_src"] = f"2 x bf16 burst ({pk['src']})"
+    try:   # library FP8 GEMM (cuBLASLt through torch) for context only
+        n = 8192
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        one = torch.ones((), device=dev)
+        for _ in range(3):
+            torch._scaled_mm(a, b.t(), one, one, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+            e0.record()
+            torch._scaled_mm(a, b.t(), one, one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        out["library_fp8_8192_tflops"] = 2.0 * n ** 3 / (best / 1e3) / 1e12
+    except Exception as exc:   # pragma: no cover - depends on the torch build
+        out["library_fp8_8192_tflops"] = None
+        out["library_fp8_note"] = str(exc)[:120]
+    return out
+
+
 # ----------------------------------------------------------------------------- GPU leg
 def main():
     args = parse()
@@ -595,6 +660,11 @@ def main():
         cpu = {"value": cv, "unit": unit, "cores": host_cores(), "kind": "oracle",
                "sample": f"{sample.desc}; {reps} passes", "seconds": tot_t}
 
+    large_m = None
+    if rank == 0 and world == 1 and w.name == "decode" and not args.no_large_m:
+        del path
+        torch.cuda.empty_cache()
+        large_m = large_m_gemms(dev, pk)
     if rank == 0:
         cfg = workload_config(w)
         line = {
@@ -606,6 +676,7 @@ def main():
             "gpu_launches": launches_per_step * args.steps,
             "step_bytes": step_bytes, "step_gemm_flops": flops, "eager_ms_per_step": eager_ms,
             "timed": "CUDA-graph replays of the whole step (eager step time in eager_ms_per_step)",
+            "large_m_gemm": large_m if large_m is not None else None,
             "per_kernel_bytes": bytes_by_kernel,
         }
         print(json.dumps(line), flush=True)
