@@ -10,4 +10,4 @@ from .ops import (  # noqa: F401
     CONTIGUOUS, MASKED, B_HOST_MAPPED, quantise_act, quantise_weight, prepare_weight_sf, route, RouteBuffers,
     route_capacity, grouped_gemm_contig, grouped_gemm_masked, combine, device_error, sf_ld, sf_words,
 )
-from .pipeline import MoEPath  # noqa: F401
+from .pipeline import MoEPath, HostStreamedPath  # noqa: F401

@@ -331,6 +331,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
         uint32_t r[32];
         tmem_ld_x32(taddr + c0, r);
         tmem_wait_ld();
+        if (c0 + 32 >= ncol) {            // last chunk is in registers: hand the accumulator back to the MMA issuer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
         // buf[j][lane] = D[token c0 + j][weight row 32q + lane]
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -350,9 +355,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
         }
         __syncwarp();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (ncol == 0) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      }
       if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
     }
   } else {

@@ -53,8 +53,9 @@ class MoEPath:
                                            expected_m=self.expected_m, flags=self.flags)
         return ops.grouped_gemm_contig(a, sfa, wq, sfb, b.seg_start, b.counts, d=d, flags=self.flags)
 
-    def step(self, x, topk_ids, topk_weights, h2=None):
-        """Run the whole path; ``h2`` is the packed bf16 [m_cap, K2] input of the second GEMM."""
+    def step(self, x, topk_ids, topk_weights, h2=None, z=None):
+        """Run the whole path; ``h2`` is the packed bf16 [m_cap, K2] input of the second GEMM;
+        the combined output goes to ``z`` (default: this object's output buffer)."""
         ops.quantise_act(x, q=self.q, sf=self.sf)
         ops.route(topk_ids, self.E, self.layout, self.align_or_max_m, q=self.q, sf=self.sf, bufs=self.bufs)
         self.gemm(self.bufs.a_packed, self.bufs.sfa_packed, self.wq, self.sfb, self.y)
@@ -63,8 +64,9 @@ class MoEPath:
             ops.quantise_act(h2, q=self.q2, sf=self.sf2)
             self.gemm(self.q2, self.sf2, self.w2q, self.sfb2, self.y2)
             out = self.y2
-        ops.combine(out, self.bufs.output_index, topk_weights, z=self.z)
-        return self.z
+        z = self.z if z is None else z
+        ops.combine(out, self.bufs.output_index, topk_weights, z=z)
+        return z
 
     def capture(self, x, topk_ids, topk_weights, h2=None):
         """Record one step on these (static) input tensors into a CUDA graph.
@@ -86,3 +88,69 @@ class MoEPath:
     def replay(self):
         self.graph.replay()
         return self.z
+
+
+class HostStreamedPath:
+    """Runs a MoEPath over batches held in pinned host memory, overlapping each
+    batch's host-to-device copy and the previous result's device-to-host copy
+    with the current step's kernels: two device input/output buffer sets, one
+    CUDA graph per set, and a copy stream ordered against the compute stream by
+    events."""
+
+    def __init__(self, path, T, K, kr, h2=None, device="cuda"):
+        self.path = path
+        self.sets = []
+        for _ in range(2):
+            dx = torch.zeros((T, K), dtype=torch.bfloat16, device=device)
+            # placeholder routing for the set-up passes: assignments spread evenly over the experts
+            dids = (torch.arange(T * kr, dtype=torch.int32, device=device) % path.E).reshape(T, kr)
+            dp = torch.full((T, kr), 1.0 / kr, dtype=torch.float32, device=device)
+            z = torch.empty_like(path.z)
+            path.step(dx, dids, dp, h2, z=z)                 # eager pass: one-time set-up outside the capture
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                path.step(dx, dids, dp, h2, z=z)
+            self.sets.append((dx, dids, dp, z, graph))
+        self.copy = torch.cuda.Stream(device=device)
+        self.h2d_done = [torch.cuda.Event() for _ in range(2)]
+        self.comp_done = [torch.cuda.Event() for _ in range(2)]
+        self.d2h_done = [torch.cuda.Event() for _ in range(2)]
+
+    def _h2d(self, k, batch):
+        dx, dids, dp, _, _ = self.sets[k]
+        hx, hids, hp = batch
+        dx.copy_(hx, non_blocking=True)
+        dids.copy_(hids, non_blocking=True)
+        dp.copy_(hp, non_blocking=True)
+        self.h2d_done[k].record(self.copy)
+
+    def run(self, host_batches, host_outputs, start_event=None, end_event=None):
+        """Process every (x, ids, weights) pinned batch into the matching pinned output."""
+        comp = torch.cuda.current_stream()
+        n = len(host_batches)
+        self.copy.wait_stream(comp)
+        with torch.cuda.stream(self.copy):
+            if start_event is not None:
+                start_event.record(self.copy)
+            self._h2d(0, host_batches[0])
+        for i in range(n):
+            k = i % 2
+            comp.wait_event(self.h2d_done[k])
+            if i >= 2:
+                comp.wait_event(self.d2h_done[k])           # output buffer k was read back
+            self.sets[k][4].replay()
+            self.comp_done[k].record(comp)
+            with torch.cuda.stream(self.copy):
+                if i + 1 < n:
+                    k2 = (i + 1) % 2
+                    if i >= 1:
+                        self.copy.wait_event(self.comp_done[k2])   # step i-1 has finished reading input set k2
+                    self._h2d(k2, host_batches[i + 1])
+                self.copy.wait_event(self.comp_done[k])
+                host_outputs[i].copy_(self.sets[k][3], non_blocking=True)
+                self.d2h_done[k].record(self.copy)
+        if end_event is not None:
+            with torch.cuda.stream(self.copy):
+                end_event.record(self.copy)
+        comp.wait_stream(self.copy)

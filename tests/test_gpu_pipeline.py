@@ -104,3 +104,24 @@ def test_graph_replay_matches_eager_step(dev, name):
                      device=dev).step(x2, ids, p)
     assert torch.equal(path.replay().view(torch.int16), expect.view(torch.int16))
     assert ops.device_error() == 0
+
+
+def test_host_streamed_path_matches_eager_steps(dev):
+    from block_scaled_fp8_route_gb300 import HostStreamedPath
+    w = W.WORKLOADS["decode"]
+    wt = W.weights(w)
+    path = MoEPath(w.E, w.kr, w.T, w.K, w.N, wt, layout=w.layout, align_or_max_m=w.max_m, device=dev)
+    batches, expect = [], []
+    for b in range(5):
+        wb = W.Workload(**{**w.__dict__, "seed": w.seed + 7 * (b + 1)})
+        x = W.activations(wb)
+        ids, p = W.routing(wb)
+        batches.append((x.pin_memory(), ids.pin_memory(), p.pin_memory()))
+        expect.append(path.step(x.to(dev), ids.to(dev), p.to(dev)).cpu())
+    streamed = HostStreamedPath(path, w.T, w.K, w.kr, device=dev)
+    outs = [torch.empty(expect[0].shape, dtype=torch.bfloat16).pin_memory() for _ in batches]
+    streamed.run(batches, outs)
+    torch.cuda.synchronize()
+    for got, exp in zip(outs, expect):
+        assert torch.equal(got.view(torch.int16), exp.view(torch.int16))
+    assert ops.device_error() == 0
