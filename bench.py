@@ -58,6 +58,22 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
 
 
+# ----------------------------------------------------------------------------- multi-rank helpers
+def max_over_ranks(value, device="cpu"):
+    """The largest value over all ranks (the slowest replica's time); identity on one rank."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def job_throughput(units_per_step, steps, world, elapsed_ms, scale):
+    """Whole-job throughput: the units every replica processed over the slowest replica's time."""
+    return units_per_step * steps * world / (elapsed_ms / 1e3) / scale
+
+
 # ----------------------------------------------------------------------------- work accounting
 def step_work(w, counts, placed_rows):
     """Algorithmic bytes and GEMM flops of one step (valid rows only; padding excluded)."""
@@ -576,11 +592,7 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    elapsed_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = tt.item()
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), dev)
     assert ops.device_error() == 0, "device error during the timed steps"
 
     gemm_ms = [a.elapsed_time(b) for a, b in gemm_events]
@@ -590,14 +602,14 @@ def main():
     launches_per_step = 1 + 4 + 1 + 1 + (2 if w.K2 else 0)
 
     if large_m:
-        value = flops * args.steps * world / (elapsed_ms / 1e3) / 1e12
+        value = job_throughput(flops, args.steps, world, elapsed_ms, 1e12)
         fp8_peak = 2.0 * pk["bf16_tflops"]           # fp8 dense = 2 x bf16 dense (nominal ratio 4.5 / 2.25)
         gflops = 2.0 * int(counts.sum()) * w.N * w.K
         achieved = gflops / (first_gemm_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak, "peak_src": f"2 x bf16 burst ({pk['src']})"}
     else:
-        value = step_bytes * args.steps * world / (elapsed_ms / 1e3) / 1e9
+        value = job_throughput(step_bytes, args.steps, world, elapsed_ms, 1e9)
         achieved = bytes_by_kernel["gemm"] / (first_gemm_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"], "peak_src": pk["src"]}
@@ -629,13 +641,9 @@ def main():
         s1 = torch.cuda.Event(enable_timing=True)
         streamed.run(seq_in, seq_out, start_event=s0, end_event=s1)
         torch.cuda.synchronize()
-        e_ms = s0.elapsed_time(s1)
-        if world > 1:
-            tt = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            e_ms = tt.item()
-        ev = (flops * args.steps * world / (e_ms / 1e3) / 1e12) if large_m else \
-            (step_bytes * args.steps * world / (e_ms / 1e3) / 1e9)
+        e_ms = max_over_ranks(s0.elapsed_time(s1), dev)
+        ev = job_throughput(flops, args.steps, world, e_ms, 1e12) if large_m else \
+            job_throughput(step_bytes, args.steps, world, e_ms, 1e9)
         e2e = {"value": ev, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / args.steps,
                "how": "pinned host batches -> device -> whole path (graph) -> pinned host output, every step; "
