@@ -43,6 +43,8 @@ def parse():
                     help="token counts of the host-weight sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-fused-dispatch", action="store_true",
+                    help="quantise + route as separate launches even where the single-launch dispatch applies")
     ap.add_argument("--no-large-m", action="store_true",
                     help="skip the large-M GEMM measurements added to the decode line")
     return ap.parse_args()
@@ -75,16 +77,21 @@ def job_throughput(units_per_step, steps, world, elapsed_ms, scale):
 
 
 # ----------------------------------------------------------------------------- work accounting
-def step_work(w, counts, placed_rows):
-    """Algorithmic bytes and GEMM flops of one step (valid rows only; padding excluded)."""
+def step_work(w, counts, placed_rows, fused_dispatch=False):
+    """Algorithmic bytes and GEMM flops of one step (valid rows only; padding excluded).
+    With the single-launch dispatch the activations are read once and only the packed
+    rows are written; otherwise the token-major quantised copy is written and re-read."""
     T, K, N, E, kr = w.T, w.K, w.N, w.E, w.kr
     R = T * kr
     nw = (K // 128 + 3) // 4
     active = [int(c) for c in counts if c > 0]
     rows = sum(active)
     b = {}
-    b["quantise"] = T * K * 2 + T * K + T * nw * 4
-    b["route"] = R * 4 + R * 4 + placed_rows * 8 + rows * (2 * K + 2 * nw * 4)
+    if fused_dispatch:
+        b["dispatch"] = T * K * 2 + R * 4 + R * 4 + placed_rows * 8 + rows * (K + nw * 4)
+    else:
+        b["quantise"] = T * K * 2 + T * K + T * nw * 4
+        b["route"] = R * 4 + R * 4 + placed_rows * 8 + rows * (2 * K + 2 * nw * 4)
     gemm_bytes = len(active) * (N * K + N * nw * 4) + rows * (K + nw * 4 + N * 2)
     flops = 2.0 * rows * N * K
     b["gemm"] = gemm_bytes
@@ -427,7 +434,7 @@ def run_host_sweep(args, w, metric):
                      "traffic": None, "kernel": "grouped_gemm_kernel"},
         "host_link": {"sm_read_gbs": link_gbs, "memcpy_h2d_gbs": memcpy_gbs},
         "sweep": sweep, "clocks": clk, "cpu_baseline": None, "e2e": None,
-        "gpu_launches": 7 * args.steps,
+        "gpu_launches": path.launches_per_step() * args.steps,
     }
     print(json.dumps(line), flush=True)
 
@@ -530,7 +537,7 @@ def main():
     a_or_m = w.max_m if w.layout == W.MASKED else w.align
     expected_m = w.T * w.kr // w.E
     path = MoEPath(w.E, w.kr, w.T, w.K, w.N, wt, layout=w.layout, align_or_max_m=a_or_m, w2_bf16=wt2,
-                   device=dev, expected_m=expected_m)
+                   device=dev, expected_m=expected_m, fused_dispatch=False if args.no_fused_dispatch else None)
     del wt, wt2
     torch.cuda.empty_cache()
     h2 = W.activations(W.with_tokens(w, path.bufs.m_cap), device=dev, K=w.K2, tag=1) if w.K2 else None
@@ -542,7 +549,7 @@ def main():
     counts = path.bufs.counts.cpu().numpy()
     placed = int(path.bufs.seg_start[-1].item())
     assert ops.device_error() == 0, "device error during setup"
-    bytes_by_kernel, flops = step_work(w, counts, placed)
+    bytes_by_kernel, flops = step_work(w, counts, placed, fused_dispatch=path.fused_dispatch)
     step_bytes = sum(bytes_by_kernel.values())
 
     for _ in range(args.warmup):
@@ -599,7 +606,7 @@ def main():
     n_gemm_per_step = 2 if w.K2 else 1
     # dominant kernel: the first (gate-up) GEMM
     first_gemm_ms = statistics.mean(gemm_ms[0::n_gemm_per_step])
-    launches_per_step = 1 + 4 + 1 + 1 + (2 if w.K2 else 0)
+    launches_per_step = path.launches_per_step()
 
     if large_m:
         value = job_throughput(flops, args.steps, world, elapsed_ms, 1e12)

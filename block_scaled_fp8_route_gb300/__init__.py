@@ -8,6 +8,6 @@ from .build import build as build_library, LIB_PATH  # noqa: F401
 from . import ops  # noqa: F401
 from .ops import (  # noqa: F401
     CONTIGUOUS, MASKED, B_HOST_MAPPED, quantise_act, quantise_weight, prepare_weight_sf, route, RouteBuffers,
-    route_capacity, grouped_gemm_contig, grouped_gemm_masked, combine, device_error, sf_ld, sf_words,
+    route_capacity, dispatch, dispatch_supported, grouped_gemm_contig, grouped_gemm_masked, combine, device_error, sf_ld, sf_words,
 )
 from .pipeline import MoEPath, HostStreamedPath  # noqa: F401

@@ -18,6 +18,7 @@
 //   route_fill    per packed row: padding marks, m_indices, row + SF copy (grid: rows)
 #include "common.cuh"
 #include "host_utils.h"
+#include "route_block.cuh"
 
 namespace bsf {
 namespace {
@@ -179,111 +180,28 @@ __global__ void __launch_bounds__(kThreads) route_assign_kernel(const int32_t* _
   if (threadIdx.x == 0 && overflow) raise_error(err, BSF_DEVERR_SEGMENT);
 }
 
-// Small batches (decode): one CTA of 1024 threads does count, scan and stable
-// ranks in one launch (the single-block routing of "CuTeDSL bei Perplexity"'s
-// decode dispatch), in rounds of 1024 assignments.
-constexpr int kSmallThreads = 1024;
-constexpr int kSmallWarps = kSmallThreads / 32;
-constexpr int kSmallMaxE = 256;
-constexpr int64_t kSmallMaxR = 16384;
-
+// Small batches (decode): one CTA routes the whole batch (route_block.cuh).
 __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const int32_t* __restrict__ ids, int64_t R,
                                                                     int kr, int E, int layout, int64_t a_or_m,
                                                                     int64_t m_cap, int32_t* __restrict__ counts,
                                                                     int32_t* __restrict__ seg_start,
                                                                     int32_t* __restrict__ output_index,
                                                                     int32_t* __restrict__ token_of_row, int* err) {
-  __shared__ int hist[kSmallMaxE];
-  __shared__ int base[kSmallMaxE];
-  __shared__ int seg[kSmallMaxE];
-  __shared__ int warp_cnt[kSmallWarps][kSmallMaxE];
-  __shared__ int warp_sums[kSmallWarps];
-  __shared__ int flags;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid < E) hist[tid] = 0;
-  if (tid == 0) flags = 0;
-  __syncthreads();
-  for (int64_t i = tid; i < R; i += kSmallThreads) {
-    const int id = ids[i];
-    if (id >= E) atomicOr(&flags, BSF_DEVERR_EXPERT_ID);
-    else if (id >= 0) atomicAdd(&hist[id], 1);
+  __shared__ RouteBlockSmem sm;
+  route_in_block(ids, R, E, layout, a_or_m, m_cap, sm, [&](int64_t i, int64_t dest) {
+    output_index[i] = static_cast<int32_t>(dest);
+    if (dest >= 0) token_of_row[dest] = static_cast<int32_t>(i / kr);
+  });
+  const int tid = threadIdx.x;
+  if (tid < E) {
+    const int M = sm.hist[tid];
+    counts[tid] = layout == BSF_LAYOUT_MASKED ? (M < a_or_m ? M : static_cast<int>(a_or_m)) : M;
+    seg_start[tid] = sm.seg[tid];
   }
-  __syncthreads();
-  // segments: masked slots, or an exclusive scan of the aligned lengths (E <= 256: 8 warps)
-  const int M = tid < E ? hist[tid] : 0;
-  if (layout == BSF_LAYOUT_MASKED) {
-    if (tid < E) {
-      const int placed = M < a_or_m ? M : static_cast<int>(a_or_m);
-      counts[tid] = placed;
-      seg[tid] = static_cast<int>(tid * a_or_m);
-      seg_start[tid] = seg[tid];
-      if (M > a_or_m) atomicOr(&flags, BSF_DEVERR_MASKED_OVERFLOW);
-    }
-    if (tid == 0) seg_start[E] = static_cast<int32_t>(E * a_or_m);
-  } else {
-    const int len = tid < E ? static_cast<int>((M + a_or_m - 1) / a_or_m * a_or_m) : 0;
-    int incl = len;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    int prefix = 0;
-    for (int w = 0; w < warp; ++w) prefix += warp_sums[w];
-    if (tid < E) {
-      seg[tid] = prefix + incl - len;
-      counts[tid] = M;
-      seg_start[tid] = seg[tid];
-      if (tid == E - 1) {
-        seg_start[E] = prefix + incl;
-        if (prefix + incl > m_cap) atomicOr(&flags, BSF_DEVERR_SEGMENT);
-      }
-    }
+  if (tid == 0) {
+    seg_start[E] = sm.seg[E];
+    if (sm.flags) raise_error(err, sm.flags);
   }
-  if (tid < E) base[tid] = 0;
-  __syncthreads();
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int64_t r0 = 0; r0 < R; r0 += kSmallThreads) {
-    for (int j = tid; j < kSmallWarps * kSmallMaxE; j += kSmallThreads) (&warp_cnt[0][0])[j] = 0;
-    __syncthreads();
-    const int64_t i = r0 + tid;
-    const int id = i < R ? ids[i] : -1;
-    const bool valid = id >= 0 && id < E;
-    const uint32_t peers = __match_any_sync(0xffffffffu, valid ? id : -1);
-    if (valid && (peers & lt_mask) == 0) warp_cnt[warp][id] = __popc(peers);
-    __syncthreads();
-    if (tid < E) {      // warp-order exclusive prefix on top of the running base
-      int run = base[tid];
-      for (int w = 0; w < kSmallWarps; ++w) {
-        const int c = warp_cnt[w][tid];
-        warp_cnt[w][tid] = run;
-        run += c;
-      }
-      base[tid] = run;
-    }
-    __syncthreads();
-    if (i < R) {
-      int64_t dest = -1;
-      if (valid) {
-        const int rank = warp_cnt[warp][id] + __popc(peers & lt_mask);
-        if (layout == BSF_LAYOUT_MASKED) {
-          if (rank < a_or_m) dest = static_cast<int64_t>(id) * a_or_m + rank;
-        } else {
-          dest = static_cast<int64_t>(seg[id]) + rank;
-        }
-        if (dest >= m_cap) {
-          dest = -1;
-          atomicOr(&flags, BSF_DEVERR_SEGMENT);
-        }
-      }
-      output_index[i] = static_cast<int32_t>(dest);
-      if (dest >= 0) token_of_row[dest] = static_cast<int32_t>(i / kr);
-    }
-    __syncthreads();
-  }
-  if (tid == 0 && flags) raise_error(err, flags);
 }
 
 constexpr int kFillRows = 32;   // packed rows per CTA in route_fill

@@ -15,6 +15,12 @@ from . import _lib
 CONTIGUOUS = 0
 MASKED = 1
 B_HOST_MAPPED = 1
+# device error bits (BSF_DEVERR_* in bsfroute.h), read with device_error()
+DEVERR_EXPERT_ID = 0x1
+DEVERR_MASKED_OVERFLOW = 0x2
+DEVERR_TIMEOUT = 0x4
+DEVERR_BAD_SCALE = 0x8
+DEVERR_SEGMENT = 0x10
 
 
 def _ptr(t):
@@ -118,6 +124,28 @@ def route(topk_ids, E, layout, align_or_max_m, q=None, sf=None, bufs=None, strea
         _ptr(bufs.a_packed) if q is not None else None, _ptr(bufs.sfa_packed) if q is not None else None,
         bufs.sfa_packed.shape[1] if (q is not None and bufs.sfa_packed is not None) else 0,
         _ptr(bufs.workspace), bufs.workspace.numel(), _stream(stream)), "route")
+    return bufs
+
+
+DISPATCH_MAX_ASSIGNMENTS = 16384
+DISPATCH_MAX_EXPERTS = 256
+
+
+def dispatch_supported(T, kr, E):
+    return T * kr <= DISPATCH_MAX_ASSIGNMENTS and E <= DISPATCH_MAX_EXPERTS
+
+
+def dispatch(x, topk_ids, E, layout, align_or_max_m, bufs=None, stream=None):
+    """Quantise + route + scatter in one launch (small batches); returns a RouteBuffers."""
+    T, K = x.shape
+    kr = topk_ids.shape[1]
+    if bufs is None:
+        bufs = RouteBuffers(T, kr, E, layout, align_or_max_m, K=K, device=x.device)
+    _lib.check(_lib.load().bsf_dispatch(
+        _ptr(x.contiguous()), T, K, _ptr(topk_ids.contiguous()), kr, E, layout, align_or_max_m,
+        _ptr(bufs.counts), _ptr(bufs.seg_start), _ptr(bufs.output_index), _ptr(bufs.token_of_row),
+        _ptr(bufs.m_indices), bufs.m_cap, _ptr(bufs.a_packed), _ptr(bufs.sfa_packed), bufs.sfa_packed.shape[1],
+        _stream(stream)), "dispatch")
     return bufs
 
 

@@ -18,7 +18,7 @@ from . import ops
 
 class MoEPath:
     def __init__(self, E, kr, T, K, N, w_bf16, layout=ops.CONTIGUOUS, align_or_max_m=1, w2_bf16=None,
-                 device="cuda", weights_on_host=False, expected_m=0):
+                 device="cuda", weights_on_host=False, expected_m=0, fused_dispatch=None):
         self.E, self.kr, self.T, self.K, self.N = E, kr, T, K, N
         self.layout, self.align_or_max_m = layout, align_or_max_m
         self.expected_m = expected_m
@@ -34,6 +34,7 @@ class MoEPath:
             self.w2q, sf2 = ops.quantise_weight(w2_bf16.to(device))
             self.sfb2 = ops.prepare_weight_sf(sf2, self.K2)
         self.bufs = ops.RouteBuffers(T, kr, E, layout, align_or_max_m, K=K, device=device)
+        self.fused_dispatch = ops.dispatch_supported(T, kr, E) if fused_dispatch is None else fused_dispatch
         m = self.bufs.m_cap
         self.q = torch.empty((T, K), dtype=torch.uint8, device=device)
         self.sf = torch.empty((ops.sf_words(K), ops.sf_ld(T)), dtype=torch.int32, device=device)
@@ -46,6 +47,18 @@ class MoEPath:
         else:
             self.z = torch.empty((T, N), dtype=torch.bfloat16, device=device)
 
+    def launches_per_step(self):
+        """Kernel launches one ``step`` makes (all of them this library's kernels)."""
+        if self.fused_dispatch:
+            n = 1                                                  # dispatch
+        else:
+            small = ops.dispatch_supported(self.T, self.kr, self.E)
+            n = 1 + (2 if small else 4)                            # quantise + route (+ fill)
+        n += 1                                                     # grouped GEMM
+        if self.two_gemms:
+            n += 2                                                 # quantise of h2 + second GEMM
+        return n + 1                                               # combine
+
     def gemm(self, a, sfa, wq, sfb, d):
         b = self.bufs
         if self.layout == ops.MASKED:
@@ -55,9 +68,13 @@ class MoEPath:
 
     def step(self, x, topk_ids, topk_weights, h2=None, z=None):
         """Run the whole path; ``h2`` is the packed bf16 [m_cap, K2] input of the second GEMM;
-        the combined output goes to ``z`` (default: this object's output buffer)."""
-        ops.quantise_act(x, q=self.q, sf=self.sf)
-        ops.route(topk_ids, self.E, self.layout, self.align_or_max_m, q=self.q, sf=self.sf, bufs=self.bufs)
+        the combined output goes to ``z`` (default: this object's output buffer).  Small batches
+        quantise, route and scatter in one launch (``dispatch``)."""
+        if self.fused_dispatch:
+            ops.dispatch(x, topk_ids, self.E, self.layout, self.align_or_max_m, bufs=self.bufs)
+        else:
+            ops.quantise_act(x, q=self.q, sf=self.sf)
+            ops.route(topk_ids, self.E, self.layout, self.align_or_max_m, q=self.q, sf=self.sf, bufs=self.bufs)
         self.gemm(self.bufs.a_packed, self.bufs.sfa_packed, self.wq, self.sfb, self.y)
         out = self.y
         if self.two_gemms:

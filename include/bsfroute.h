@@ -186,6 +186,34 @@ bsf_status bsf_route_no_alloc(const int32_t* topk_ids, int64_t T, int64_t kr, in
                               int64_t sfa_ld, bsf_stream_t stream);
 
 /*
+ * bsf_dispatch — quantise + route + scatter in ONE launch, for small batches
+ * (decode): T*kr <= BSF_DISPATCH_MAX_ASSIGNMENTS and E <=
+ * BSF_DISPATCH_MAX_EXPERTS, else BSF_ERR_UNSUPPORTED (use bsf_quantise_act +
+ * bsf_route).
+ * "CuTeDSL bei Perplexity", MoE dispatch (decode: one block holds all the
+ * routing information; routing and copies in one launch).  Every CTA routes
+ * the whole batch in shared memory, then quantises its share of the routed
+ * rows straight from x into their packed rows, so no grid-wide barrier is
+ * needed.  Outputs are bit-identical to bsf_quantise_act followed by
+ * bsf_route with the scatter (same arguments and layouts as those two; the
+ * token-major q / sf copies are not produced).
+ *   x             bf16 [T, K], K % 128 == 0 (device, caller-owned, read only).
+ *   a_packed      e4m3 [m_cap, K]; sfa_packed int32 [ceil(K/512)][sfa_ld]
+ *                 (device, caller-owned): routed rows written, padding rows
+ *                 left as they were.
+ *   other arguments, the device error bits (EXPERT_ID, MASKED_OVERFLOW,
+ *   SEGMENT) and the host-side checks are as in bsf_route; x, a_packed and
+ *   sfa_packed must be 16-byte aligned (BSF_ERR_MISALIGNED).  Nothing is
+ *   allocated; the call is asynchronous on `stream`.
+ */
+#define BSF_DISPATCH_MAX_ASSIGNMENTS 16384
+#define BSF_DISPATCH_MAX_EXPERTS 256
+bsf_status bsf_dispatch(const void* x, int64_t T, int64_t K, const int32_t* topk_ids, int64_t kr, int64_t E,
+                        int layout, int64_t align_or_max_m, int32_t* counts, int32_t* seg_start,
+                        int32_t* output_index, int32_t* token_of_row, int32_t* m_indices, int64_t m_cap,
+                        uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld, bsf_stream_t stream);
+
+/*
  * bsf_grouped_gemm_contig — D[r, :] = BF16( dequant(A[r, :]) . dequant(B_e)^T )
  * for every expert e and every row r in [seg_start[e], seg_start[e] + counts[e]).
  * "GEMM 执行方式" §4.1 (P independent problems), §4.4 (Y_e = X_e W_e^T);

@@ -42,3 +42,23 @@ def test_argument_validation_needs_no_device(lib):
                          nul) == 1
     # combine with N not a multiple of 8
     assert lib.bsf_combine(nul, 4, nul, nul, 2, 2, 12, nul, nul) == 1
+    # dispatch: batch above the single-launch limit is unsupported, K not a multiple of 128 invalid
+    assert lib.bsf_dispatch(nul, 4096, 128, nul, 8, 128, 0, 1, nul, nul, nul, nul, nul, 1 << 20, nul, nul, 1 << 20,
+                            nul) == 3
+    assert lib.bsf_dispatch(nul, 4, 100, nul, 2, 4, 0, 1, nul, nul, nul, nul, nul, 8, nul, nul, 8, nul) == 1
+
+
+def test_python_constants_match_header():
+    import os
+    import re
+
+    from block_scaled_fp8_route_gb300 import ops
+    with open(os.path.join(build.ROOT, "include", "bsfroute.h")) as f:
+        text = f.read()
+    defs = {m.group(1): int(m.group(2), 0) for m in re.finditer(r"#define BSF_(\w+) (0x[0-9a-fA-F]+|\d+)", text)}
+    for name in ("DEVERR_EXPERT_ID", "DEVERR_MASKED_OVERFLOW", "DEVERR_TIMEOUT", "DEVERR_BAD_SCALE",
+                 "DEVERR_SEGMENT"):
+        assert getattr(ops, name) == defs[name], name
+    assert ops.B_HOST_MAPPED == defs["B_HOST_MAPPED"]
+    assert ops.DISPATCH_MAX_ASSIGNMENTS == defs["DISPATCH_MAX_ASSIGNMENTS"]
+    assert ops.DISPATCH_MAX_EXPERTS == defs["DISPATCH_MAX_EXPERTS"]
