@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
   __shared__ int share_tok[kMaxShare];
   __shared__ int share_dest[kMaxShare];
   __shared__ int n_share;
+  pdl_launch_dependents();     // a dependent GEMM may be scheduled now; it waits for completion
   const int64_t R = T * kr;
   const int G = gridDim.x, b = blockIdx.x;
   if (threadIdx.x == 0) n_share = 0;

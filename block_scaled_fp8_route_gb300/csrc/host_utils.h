@@ -17,6 +17,34 @@ inline bsf_status launch_status() {
   return err == cudaSuccess ? BSF_OK : BSF_ERR_CUDA;
 }
 
+// Launch `kernel` as a programmatic dependent of the preceding kernel on `stream`
+// (cudaLaunchAttributeProgrammaticStreamSerialization): its CTAs may be scheduled while
+// that kernel drains, and it must call pdl_wait() before its first global memory access.
+// Returns the launch's configuration status.
+template <class... Params, class... Args>
+inline bsf_status launch_dependent(void (*kernel)(Params...), unsigned grid, unsigned block, size_t smem,
+                                   cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+#ifdef BSF_DISABLE_PDL
+  cfg.numAttrs = 0;
+#else
+  cfg.numAttrs = 1;
+#endif
+  if (cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    return BSF_ERR_CUDA;
+  }
+  return launch_status();
+}
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

@@ -17,6 +17,7 @@ namespace {
 __global__ void __launch_bounds__(256) quantise_act_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t K,
                                                            uint8_t* __restrict__ q, int32_t* __restrict__ sf,
                                                            int64_t sf_ld) {
+  pdl_launch_dependents();     // a dependent GEMM may be scheduled now; it waits for completion
   const int64_t n_groups = (K + 511) / 512;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;

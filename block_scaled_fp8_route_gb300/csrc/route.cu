@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(kThreads) route_fill_kernel(int E, int64_t m_c
                                                               const int32_t* __restrict__ sf, int64_t sf_ld, int64_t K,
                                                               uint8_t* __restrict__ a_packed,
                                                               int32_t* __restrict__ sfa_packed, int64_t sfa_ld) {
+  pdl_launch_dependents();     // a dependent GEMM may be scheduled now; it waits for completion
   __shared__ int tok[kFillRows];
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kFillRows;
   const int64_t rows_used = seg_start[E];

@@ -214,6 +214,12 @@ bsf_status bsf_dispatch(const void* x, int64_t T, int64_t K, const int32_t* topk
                         uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld, bsf_stream_t stream);
 
 /*
+ * Launch order: every call is stream-ordered.  The small-batch tile
+ * (bsf_grouped_gemm_masked with max_m <= 64, or with expected_m <= 32 and
+ * device-resident weights) is launched as a programmatic dependent
+ * of the preceding kernel on the stream: its CTAs may be scheduled while that
+ * kernel drains, and they touch no global memory until it has completed.
+ *
  * bsf_grouped_gemm_contig — D[r, :] = BF16( dequant(A[r, :]) . dequant(B_e)^T )
  * for every expert e and every row r in [seg_start[e], seg_start[e] + counts[e]).
  * "GEMM 执行方式" §4.1 (P independent problems), §4.4 (Y_e = X_e W_e^T);

@@ -81,3 +81,45 @@ def test_dispatch_reports_overflow_bad_ids_and_rejects_large_batches(dev):
     big = torch.zeros((4096, 128), dtype=torch.bfloat16, device=dev)
     with pytest.raises(_lib.BsfError):
         ops.dispatch(big, torch.zeros((4096, 8), dtype=torch.int32, device=dev), 128, ops.CONTIGUOUS, 1)
+
+
+def test_dependent_gemm_sees_the_dispatch_of_the_same_step(dev):
+    """The small-batch GEMM starts as a programmatic dependent of the dispatch before it; back-to-back
+    steps on alternating batches must give exactly what the same calls give with a full
+    synchronisation between every launch."""
+    E, K, N, T, kr, max_m = 16, 512, 256, 64, 4, 64
+    g = torch.Generator().manual_seed(7)
+    batches = []
+    for _ in range(2):
+        x = torch.randn(T, K, generator=g).to(torch.bfloat16).to(dev)
+        ids = torch.stack([torch.randperm(E, generator=g)[:kr] for _ in range(T)]).to(torch.int32).to(dev)
+        batches.append((x, ids))
+    wq, sf128 = ops.quantise_weight((torch.randn(E, N, K, generator=g) * 0.02).to(torch.bfloat16).to(dev))
+    sfb = ops.prepare_weight_sf(sf128, K)
+
+    def step(x, ids, bufs, d, sync):
+        ops.dispatch(x, ids, E, ops.MASKED, max_m, bufs=bufs)
+        if sync:
+            torch.cuda.synchronize()
+        ops.grouped_gemm_masked(bufs.a_packed, bufs.sfa_packed, wq, sfb, bufs.counts, max_m, d=d, expected_m=16)
+        if sync:
+            torch.cuda.synchronize()
+
+    bufs = ops.RouteBuffers(T, kr, E, ops.MASKED, max_m, K=K, device=dev)
+    d = torch.empty((E * max_m, N), dtype=torch.bfloat16, device=dev)
+    refs = []
+    for x, ids in batches:
+        step(x, ids, bufs, d, sync=True)
+        refs.append((d.clone(), bufs.counts.clone()))
+    outs = []
+    for i in range(20):
+        x, ids = batches[i % 2]
+        step(x, ids, bufs, d, sync=False)
+        outs.append(d.clone())                     # stream-ordered copy after the GEMM
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    for i, out in enumerate(outs):
+        ref, counts = refs[i % 2]
+        for e in range(E):
+            rows = slice(e * max_m, e * max_m + int(counts[e]))
+            assert torch.equal(out[rows].view(torch.int16), ref[rows].view(torch.int16)), (i, e)
