@@ -669,6 +669,16 @@ def main():
         cpu = {"value": cv, "unit": unit, "cores": host_cores(), "kind": "oracle",
                "sample": f"{sample.desc}; {reps} passes", "seconds": tot_t}
 
+    # context: the rate at which the SMs stream-read HBM alone (this library's checksum kernel over
+    # 4 GiB); the roofline's denominator stays the measured copy bandwidth
+    hbm_read = None
+    if rank == 0 and not large_m:
+        probe = torch.empty(4 << 30, dtype=torch.uint8, device=dev)
+        probe.fill_(1)
+        hbm_read = measure_read_gbs(probe, False)
+        del probe
+        torch.cuda.empty_cache()
+
     large_m = None
     if rank == 0 and world == 1 and w.name == "decode" and not args.no_large_m:
         del path
@@ -687,6 +697,7 @@ def main():
             "timed": "CUDA-graph replays of the whole step (eager step time in eager_ms_per_step)",
             "large_m_gemm": large_m if large_m is not None else None,
             "per_kernel_bytes": bytes_by_kernel,
+            "hbm_stream_read_gbs": hbm_read,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

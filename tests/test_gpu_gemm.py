@@ -85,6 +85,20 @@ def test_masked_ragged(dev, max_m, expected_m):
     _check_all(d, ref_ops, seg, masked, f"masked max_m={max_m}")
 
 
+def test_masked_many_experts_small_slots(dev):
+    """More than 256 experts with small slots: the small-batch tile with its 1024-expert tables."""
+    rng = np.random.default_rng(5)
+    E, N, K, max_m = 260, 128, 128, 32
+    masked = rng.integers(0, max_m + 1, E)
+    masked[:7] = 0
+    (aq, asf, bq, sfb), ref_ops = _operands(E * max_m, E, N, K, 77, dev)
+    d = torch.full((E * max_m, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    ops.grouped_gemm_masked(aq, asf, bq, sfb, torch.as_tensor(masked, dtype=torch.int32, device=dev), max_m, d=d)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    _check_all(d, ref_ops, np.arange(E + 1) * max_m, masked, "masked E=260")
+
+
 def test_grouped_equals_single_launches_bitwise(dev):
     counts = np.array([40, 0, 130, 7])
     E, N, K = 4, 256, 512
