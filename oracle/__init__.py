@@ -16,7 +16,10 @@ Sources (page title, section):
   "FP8 的精度陷阱" (E4M3 format), "补偿机制一" (power-of-two scale factors,
   UE8M0 packing), "补偿机制三" (MN-major packed SF layout), "精度与吞吐的平衡点"
   (calc_diff tolerance, repeat-run determinism).
-* "AsymGEMM" README, "Token Layout Protocols" (contiguous and masked layouts).
+* "AsymGEMM" README, "Token Layout Protocols" (contiguous and masked layouts),
+  "FP4 Asymmetric GEMM" (NVFP4 operands, ``oracle/nvfp4.py``).
+* "CuTeDSL bei Perplexity", Blackwell support (16-element absolute maximum
+  of the NVFP4 quantiser).
 
 Pinning status of each function is stated in its module docstring.  Every
 function is pinned by at least one test in ``tests/test_oracle_*.py`` against
@@ -24,4 +27,4 @@ values the pages print, closed forms, library routines or brute force, except
 the GPU-internal FP32 accumulation order, which is outside the oracle.
 """
 
-from . import formats, quantise, route, gemm, combine, checks  # noqa: F401
+from . import formats, quantise, route, gemm, combine, checks, nvfp4  # noqa: F401

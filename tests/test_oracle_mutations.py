@@ -89,3 +89,47 @@ def test_dropped_routing_weight_is_caught(monkeypatch, golden_dir):
 
     monkeypatch.setattr(combine, "combine", unweighted)
     _fails(pin_combine.test_page_formula_z0, golden_dir)
+
+
+# ---------------------------------------------------------------- NVFP4
+from oracle import nvfp4  # noqa: E402
+from tests import test_oracle_nvfp4 as pin_nvfp4  # noqa: E402
+
+
+def test_swapped_nibbles_are_caught(monkeypatch):
+    orig = nvfp4.unpack_e2m1
+
+    def swapped(packed):
+        c = orig(packed)
+        out = c.copy()
+        out[..., 0::2], out[..., 1::2] = c[..., 1::2], c[..., 0::2]
+        return out
+
+    monkeypatch.setattr(nvfp4, "unpack_e2m1", swapped)
+    # (a dot product is blind to the same swap on both operands; the byte-level pin is not)
+    _fails(pin_nvfp4.test_nibble_and_sf_byte_order)
+
+
+def test_e2m1_ties_away_from_zero_are_caught(monkeypatch):
+    orig = nvfp4.e2m1_encode
+    monkeypatch.setattr(nvfp4, "e2m1_encode", lambda y: orig(np.asarray(y, dtype=np.float64) * (1 + 2 ** -30)))
+    _fails(pin_nvfp4.test_e2m1_ties_to_even_and_saturation)
+
+
+def test_wrong_scale_divisor_is_caught(monkeypatch):
+    monkeypatch.setattr(nvfp4, "quantise_rows", _scaled_divisor(nvfp4.quantise_rows))
+    _fails(pin_nvfp4.test_hand_computed_blocks)
+
+
+def _scaled_divisor(orig):
+    def wrong(x_bits, j):
+        # scales from amax / 4 instead of amax / 6: the same as quantising x * 1.5
+        x = nvfp4.formats.bf16_bits_to_f64(x_bits) * 1.5
+        return orig(nvfp4.formats.bf16_round(x), j)
+    return wrong
+
+
+def test_global_exponent_off_by_one_is_caught(monkeypatch):
+    orig = nvfp4.global_exponent
+    monkeypatch.setattr(nvfp4, "global_exponent", lambda a: orig(a) + 1)
+    _fails(pin_nvfp4.test_global_exponent_is_least)
