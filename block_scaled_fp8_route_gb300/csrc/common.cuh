@@ -155,6 +155,19 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// NVFP4: E2M1 operands, one UE4M3 scale per 16 K (four per K = 64 step, one
+// 32-bit TMEM word per row).
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
                "r"(v2), "r"(v3)
@@ -209,6 +222,17 @@ __device__ __forceinline__ uint32_t idesc_mxf8_e4m3(uint32_t m, uint32_t n, uint
   d |= 1u << 23;              // scale factor type UE8M0
   d |= (m >> 4) << 24;        // M / 16
   d |= (a_sf & 3u) << 29;     // A scale factor id
+  return d;
+}
+
+// Instruction descriptor for kind::mxf4nvf4 with scale_vec::4X: A and B E2M1
+// (format 1), K-major, UE4M3 scales (bit 23 clear), no scale-factor ids.
+__device__ __forceinline__ uint32_t idesc_nvf4(uint32_t m, uint32_t n) {
+  uint32_t d = 0;
+  d |= 1u << 7;               // A format E2M1
+  d |= 1u << 10;              // B format E2M1
+  d |= (n >> 3) << 17;        // N / 8
+  d |= (m >> 4) << 24;        // M / 16
   return d;
 }
 

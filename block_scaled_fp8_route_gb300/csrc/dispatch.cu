@@ -21,11 +21,15 @@ constexpr int kMaxShare = 1024;   // routed assignments one CTA may own
 static_assert(kSmallMaxR == BSF_DISPATCH_MAX_ASSIGNMENTS && kSmallMaxE == BSF_DISPATCH_MAX_EXPERTS,
               "single-launch limits out of sync with the header");
 
+// FP4 = false: E4M3 rows with one UE8M0 byte per 128 values (bsf_quantise_act);
+// FP4 = true: NVFP4 rows (K/2 bytes) with one UE4M3 byte per 16 values and
+// tensor exponent a_exp (bsf_quantise_act_nvfp4).
+template <bool FP4>
 __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
     const uint16_t* __restrict__ x, int64_t T, int64_t K, const int32_t* __restrict__ ids, int kr, int E, int layout,
     int64_t a_or_m, int64_t m_cap, int32_t* __restrict__ counts, int32_t* __restrict__ seg_start,
     int32_t* __restrict__ output_index, int32_t* __restrict__ token_of_row, int32_t* __restrict__ m_indices,
-    uint8_t* __restrict__ a_packed, int32_t* __restrict__ sfa_packed, int64_t sfa_ld, int* err) {
+    uint8_t* __restrict__ a_packed, int32_t* __restrict__ sfa_packed, int64_t sfa_ld, int a_exp, int* err) {
   __shared__ RouteBlockSmem sm;
   __shared__ int share_tok[kMaxShare];
   __shared__ int share_dest[kMaxShare];
@@ -92,8 +96,22 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
         v[j] = fa[j];
         v[8 + j] = fb[j];
       }
+      if constexpr (!FP4) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+      }
+    }
+    if constexpr (FP4) {
+      // lane = one 16-value block: 8 bytes of codes, one scale byte; lanes 4m..4m+3 form scale word m
+      uint32_t lo = 0, hi = 0, code = 0;
+      if (active) code = nvfp4_block(v, a_exp, lo, hi);
+      if (active) *reinterpret_cast<uint2*>(a_packed + dest * (K / 2) + k0 / 2) = make_uint2(lo, hi);
+      const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 1);
+      const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 2);
+      const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 3);
+      if (active && (lane & 3) == 0)
+        sfa_packed[(k0 / 64) * sfa_ld + dest] = static_cast<int32_t>(code | (c1 << 8) | (c2 << 16) | (c3 << 24));
+      continue;
     }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
@@ -122,13 +140,17 @@ __global__ void __launch_bounds__(kSmallThreads) dispatch_small_kernel(
 
 using namespace bsf;
 
-extern "C" bsf_status bsf_dispatch(const void* x, int64_t T, int64_t K, const int32_t* topk_ids, int64_t kr, int64_t E,
-                                   int layout, int64_t align_or_max_m, int32_t* counts, int32_t* seg_start,
-                                   int32_t* output_index, int32_t* token_of_row, int32_t* m_indices, int64_t m_cap,
-                                   uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld, bsf_stream_t stream) {
-  if (T < 0 || kr <= 0 || E <= 0 || K <= 0 || K % 128) return BSF_ERR_INVALID_ARGUMENT;
+namespace bsf {
+namespace {
+
+template <bool FP4>
+bsf_status launch_dispatch(const void* x, int64_t T, int64_t K, const int32_t* topk_ids, int64_t kr, int64_t E,
+                           int layout, int64_t align_or_max_m, int32_t* counts, int32_t* seg_start,
+                           int32_t* output_index, int32_t* token_of_row, int32_t* m_indices, int64_t m_cap,
+                           uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld, int a_exp, bsf_stream_t stream) {
+  if (T < 0 || kr <= 0 || E <= 0 || K <= 0 || K % (FP4 ? 64 : 128)) return BSF_ERR_INVALID_ARGUMENT;
   if (layout != BSF_LAYOUT_CONTIGUOUS && layout != BSF_LAYOUT_MASKED) return BSF_ERR_INVALID_ARGUMENT;
-  if (align_or_max_m < 1) return BSF_ERR_INVALID_ARGUMENT;
+  if (align_or_max_m < 1 || a_exp < -100 || a_exp > 100) return BSF_ERR_INVALID_ARGUMENT;
   const int64_t R = T * kr;
   if (R > kSmallMaxR || E > kSmallMaxE) return BSF_ERR_UNSUPPORTED;
   if (!x || !topk_ids || !counts || !seg_start || !output_index || !token_of_row || !a_packed || !sfa_packed)
@@ -145,9 +167,29 @@ extern "C" bsf_status bsf_dispatch(const void* x, int64_t T, int64_t K, const in
   if (grid < min_grid) grid = min_grid;
   if (R > 0 && grid > R) grid = R;
   if (grid < 1) grid = 1;
-  dispatch_small_kernel<<<static_cast<unsigned>(grid), kSmallThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+  dispatch_small_kernel<FP4><<<static_cast<unsigned>(grid), kSmallThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint16_t*>(x), T, K, topk_ids, static_cast<int>(kr), static_cast<int>(E), layout,
       align_or_max_m, m_cap, counts, seg_start, output_index, token_of_row, m_indices, a_packed, sfa_packed, sfa_ld,
-      err);
+      a_exp, err);
   return launch_status();
+}
+
+}  // namespace
+}  // namespace bsf
+
+extern "C" bsf_status bsf_dispatch(const void* x, int64_t T, int64_t K, const int32_t* topk_ids, int64_t kr, int64_t E,
+                                   int layout, int64_t align_or_max_m, int32_t* counts, int32_t* seg_start,
+                                   int32_t* output_index, int32_t* token_of_row, int32_t* m_indices, int64_t m_cap,
+                                   uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld, bsf_stream_t stream) {
+  return launch_dispatch<false>(x, T, K, topk_ids, kr, E, layout, align_or_max_m, counts, seg_start, output_index,
+                                token_of_row, m_indices, m_cap, a_packed, sfa_packed, sfa_ld, 0, stream);
+}
+
+extern "C" bsf_status bsf_dispatch_nvfp4(const void* x, int64_t T, int64_t K, int a_exp, const int32_t* topk_ids,
+                                         int64_t kr, int64_t E, int layout, int64_t align_or_max_m, int32_t* counts,
+                                         int32_t* seg_start, int32_t* output_index, int32_t* token_of_row,
+                                         int32_t* m_indices, int64_t m_cap, uint8_t* a_packed, int32_t* sfa_packed,
+                                         int64_t sfa_ld, bsf_stream_t stream) {
+  return launch_dispatch<true>(x, T, K, topk_ids, kr, E, layout, align_or_max_m, counts, seg_start, output_index,
+                               token_of_row, m_indices, m_cap, a_packed, sfa_packed, sfa_ld, a_exp, stream);
 }

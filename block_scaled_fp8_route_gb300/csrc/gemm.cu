@@ -40,6 +40,9 @@ constexpr int kMaxExperts = 1024;
 constexpr int kThreads = 320;
 constexpr int kBigTok = 224;        // token tile of the large-segment variant
 constexpr int kHostTok = 448;       // token tile of the host-weight (K-outer / M-inner) variant
+constexpr int kFmtFp8 = 0;          // E4M3 operands, UE8M0 scales per 128 K (kind::mxf8f6f4, 1X)
+constexpr int kFmtNvfp4 = 1;        // E2M1 operands, UE4M3 scales per 16 K (kind::mxf4nvf4, 4X)
+constexpr int kNvfp4MaxE = 256;     // NVFP4 variants size their tile tables for 256 experts
 
 struct GemmArgs {
   const int32_t* seg_start;  // contiguous: [E+1]; masked: nullptr
@@ -53,6 +56,8 @@ struct GemmArgs {
   int E, N, K;
   int* err;
   int withhold_loads;        // test-only fault injection (BSF_DEBUG_WITHHOLD_LOADS)
+  int a_exp;                 // NVFP4: tensor exponent of A
+  const int32_t* b_exp;      // NVFP4: tensor exponent per expert of B [E]
 };
 
 // TOK = token columns of one tile's accumulator.  64 and 224 keep two
@@ -68,14 +73,23 @@ struct GemmArgs {
 // by the other's MMAs.
 // MAXE = the most experts the per-CTA tile tables hold; the small-batch tile with at most 256
 // experts turns the table space it saves into a fourth pipeline stage (-1.4 % at decode).
-template <int TOK, int CPS = 1, int MAXE = kMaxExperts>
+// FMT = operand format.  A stage is always 128 bytes of K per row: 128 FP8
+// values (four K = 32 MMAs) or 256 NVFP4 values (four K = 64 MMAs).  FP8
+// scale words cover four stages (one byte per stage, picked by sf_id);
+// NVFP4 needs a word per row per MMA, so its SF slot covers one stage:
+// 4 x 4 weight columns + 4 x 4 token columns (tokens <= 128).
+template <int TOK, int CPS = 1, int MAXE = kMaxExperts, int FMT = kFmtFp8>
 struct Cfg {
+  static constexpr bool kFp4 = FMT == kFmtNvfp4;
   static constexpr int kMaxE = MAXE;
-  static constexpr int kStages = CPS == 2 ? (TOK <= 64 ? (MAXE <= 256 ? 4 : 3) : 2) : TOK <= 64 ? 8 : TOK <= 224 ? 4 : 2;
+  static constexpr int kKElems = kFp4 ? 256 : 128;           // K values per stage
+  static constexpr int kKbPerSlot = kFp4 ? 1 : 4;            // stages per SF slot
+  static constexpr int kStages = CPS == 2 ? (TOK <= 64 ? (MAXE <= 256 ? 4 : 3) : TOK <= 128 ? 3 : 2)
+                                          : TOK <= 64 ? 8 : TOK <= 224 ? 4 : 2;
   static constexpr int kAccBufs = (CPS == 1 && TOK <= 224) ? 2 : 1;
-  static constexpr int kSfSlots = (CPS == 1 && TOK <= 224) ? 4 : 2;
+  static constexpr int kSfSlots = kFp4 ? 4 : (CPS == 1 && TOK <= 224) ? 4 : 2;
   static constexpr int kTokSfCols = (TOK + 31) / 32;
-  static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK <= 224 ? 56 : 224;   // token rows per TMA box
+  static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK <= 128 ? 64 : TOK <= 224 ? 56 : 224;   // token rows per TMA box
   // Launched as a programmatic dependent of the preceding kernel (dispatch / route / quantise)
   // only for the small-batch tile: there the launch and prologue overlap that kernel's tail
   // (-0.9 us per graph-replayed decode step, -2 us eager).  The large-tile variants lost
@@ -88,7 +102,7 @@ struct Cfg {
   // SF slot: 4 weight-SF columns, then per sub-tile kSub/32 token-SF columns
   // starting every 8 columns (scale-factor TMEM addresses stay 4-column aligned)
   static constexpr int kSubSfCols = kSub / 32;
-  static constexpr int kSfCols = TOK <= 64 ? 8 : TOK <= 224 ? 16 : 32;
+  static constexpr int kSfCols = kFp4 ? 32 : TOK <= 64 ? 8 : TOK <= 224 ? 16 : 32;
   static __device__ __forceinline__ int tok_sf_col(int c) { return 4 + (c / kSubSfCols) * 8 + c % kSubSfCols; }
   static constexpr int kSfBase = kAccBufs * TOK;
   static constexpr int kTmemUsed = kSfBase + kSfSlots * kSfCols;
@@ -111,11 +125,18 @@ struct Cfg {
   static_assert(TOK % kBoxRows == 0, "whole TMA boxes must fit the token stage");
   static_assert(kSub % 32 == 0 && (kSub * kBlockK) % 1024 == 0, "sub-tile alignment");
   static_assert((kBoxRows * kBlockK) % 1024 == 0, "TMA boxes must keep the 1024-byte swizzle alignment");
+  static_assert(!kFp4 || (TOK <= 128 && MAXE <= kNvfp4MaxE), "NVFP4 tiles: at most 128 tokens, 256 experts");
 };
 
 struct Tile {
   int e, nt, tok0, ntok;
 };
+
+// 2**j for j clamped to [-100, 100] (exact).
+__device__ __forceinline__ float exp2_int(int j) {
+  j = j < -100 ? -100 : (j > 100 ? 100 : j);
+  return __uint_as_float(static_cast<uint32_t>(127 + j) << 23);
+}
 
 __device__ __forceinline__ Tile decode_tile(int t, const int* tile_start, const int* row0, const int* cnt, int E,
                                             int nnt, int tok) {
@@ -154,11 +175,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int TOK, int CPS, int MAXE>
+template <int TOK, int CPS, int MAXE, int FMT>
 __global__ void __launch_bounds__(kThreads, CPS)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_a,
                         const GemmArgs p) {
-  using C = Cfg<TOK, CPS, MAXE>;
+  using C = Cfg<TOK, CPS, MAXE, FMT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_b = smem;
@@ -182,8 +203,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
   const int lane = threadIdx.x & 31;
   const int E = p.E, N = p.N;
   const int nnt = N / kBlockW;
-  const int nkb = p.K / kBlockK;
-  const int nw = (nkb + 3) / 4;
+  const int nkb = p.K / C::kKElems;
+  const int nw = C::kFp4 ? p.K / 64 : (nkb + 3) / 4;        // SF words per row
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -301,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * TOK;
         for (int kb = 0; kb < nkb; ++kb) {
-          if ((kb & 3) == 0) {
+          if (kb % C::kKbPerSlot == 0) {
             if (!mbar_wait(&sf_full[sf_slot], sf_phase, abort_flag, p.err)) { ok = false; break; }
           }
           if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
@@ -310,6 +331,13 @@ __global__ void __launch_bounds__(kThreads, CPS)
           const uint32_t sft = sfw + 4;
           const uint64_t adesc = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB));
           const uint64_t bdesc = smem_desc_k_sw128(smem_u32(stage_a + stage * C::kStageA));
+          if constexpr (C::kFp4) {
+            // four K = 64 steps; step k's scales: weight words at columns 4k, token words at 16 + 4k
+            const uint32_t idesc = idesc_nvf4(kBlockW, mma_n);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_nvf4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sfw + 4 * k, sfw + 16 + 4 * k, (kb | k) != 0);
+          } else {
           // sub-tiles of at most kSub tokens: columns j*kSub.., smem rows j*kSub.., token SF columns j*kSub/32..
 #pragma unroll
           for (int j = 0; j < TOK / C::kSub; ++j) {
@@ -323,9 +351,10 @@ __global__ void __launch_bounds__(kThreads, CPS)
               mma_mxf8(d_tmem + j * C::kSub, adesc + 2 * k, bd + 2 * k, idesc, sfw, sft + j * 8, (kb | k) != 0);
             }
           }
+          }
           tc_commit(&empty[stage]);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-          if ((kb & 3) == 3 || kb == nkb - 1) {
+          if (kb % C::kKbPerSlot == C::kKbPerSlot - 1 || kb == nkb - 1) {
             tc_commit(&sf_empty[sf_slot]);
             if (++sf_slot == C::kSfSlots) { sf_slot = 0; sf_phase ^= 1u; }
           }
@@ -350,6 +379,12 @@ __global__ void __launch_bounds__(kThreads, CPS)
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * TOK;
       const int ncol = (tl.ntok + 31) & ~31;
+      // NVFP4: the tensor scales 2**a_exp * 2**b_exp[e], applied exactly (two power-of-two products)
+      float alpha_a = 1.f, alpha_b = 1.f;
+      if constexpr (C::kFp4) {
+        alpha_a = exp2_int(p.a_exp);
+        alpha_b = exp2_int(p.b_exp ? p.b_exp[tl.e] : 0);
+      }
       for (int c0 = 0; c0 < ncol; c0 += 32) {
         uint32_t r[32];
         tmem_ld_x32(taddr + c0, r);
@@ -362,7 +397,9 @@ __global__ void __launch_bounds__(kThreads, CPS)
         // buf[j][lane] = D[token c0 + j][weight row 32q + lane]
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(r[j]));
+          float v = __uint_as_float(r[j]);
+          if constexpr (C::kFp4) v = v * alpha_a * alpha_b;
+          const __nv_bfloat16 h = __float2bfloat16_rn(v);
           buf[j * 32 + lane] = *reinterpret_cast<const uint16_t*>(&h);
         }
         __syncwarp();
@@ -392,6 +429,48 @@ __global__ void __launch_bounds__(kThreads, CPS)
     const int q = warp & 3;
     uint32_t sf_slot = 0, sf_phase = 0;
     bool ok = true;
+    if constexpr (C::kFp4) {
+      // NVFP4: per stage, MMA k's word of weight row (lane + 32c) -> column 4k + c, of token
+      // row (lane + 32c) -> column 16 + 4k + c; rows past the tile get scale 0
+      for (int t = t_first; t < total_tiles && ok; t += G) {
+        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
+        const int mma_n = (tl.ntok + 15) & ~15;
+        const int32_t* sfb_base = p.sfb + static_cast<int64_t>(tl.e) * nw * N + tl.nt * kBlockW + lane;
+        for (int kb = 0; kb < nkb; ++kb) {
+          uint32_t w[4][4];
+          uint32_t a[4][C::kTokSfCols];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int64_t word = static_cast<int64_t>(kb) * 4 + k;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) w[k][c] = static_cast<uint32_t>(__ldg(sfb_base + word * N + 32 * c));
+#pragma unroll
+            for (int c = 0; c < C::kTokSfCols; ++c) {
+              const int rl = lane + 32 * c;
+              const int64_t row = static_cast<int64_t>(tl.tok0) + rl;
+              a[k][c] = (rl < mma_n && row < p.m_rows) ? static_cast<uint32_t>(__ldg(p.sfa + word * p.sfa_ld + row))
+                                                       : 0u;
+            }
+          }
+          if (!warp_wait(&sf_empty[sf_slot], sf_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t col =
+              tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::kSfBase + sf_slot * C::kSfCols;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tmem_st_x4(col + 4 * k, w[k][0], w[k][1], w[k][2], w[k][3]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+#pragma unroll
+            for (int c = 0; c < C::kTokSfCols; ++c) tmem_st_x1(col + 16 + 4 * k + c, a[k][c]);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sf_full[sf_slot]);
+          if (++sf_slot == C::kSfSlots) { sf_slot = 0; sf_phase ^= 1u; }
+        }
+      }
+    } else
     for (int t = t_first; t < total_tiles && ok; t += G) {
       const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
       const int mma_n = (tl.ntok + 15) & ~15;
@@ -458,21 +537,22 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int TOK, int CPS = 1, int MAXE = kMaxExperts>
+template <int TOK, int CPS = 1, int MAXE = kMaxExperts, int FMT = kFmtFp8>
 bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int64_t max_tiles, cudaStream_t s) {
-  using C = Cfg<TOK, CPS, MAXE>;
+  using C = Cfg<TOK, CPS, MAXE, FMT>;
   if (args.E > MAXE) return BSF_ERR_UNSUPPORTED;
   CUtensorMap map_a, map_b;
-  if (!make_map(&map_a, a, args.m_rows, args.K, C::kBoxRows)) return BSF_ERR_CUDA;
-  if (!make_map(&map_b, b, static_cast<int64_t>(args.E) * args.N, args.K, kBlockW)) return BSF_ERR_CUDA;
+  const int64_t row_bytes = C::kFp4 ? args.K / 2 : args.K;
+  if (!make_map(&map_a, a, args.m_rows, row_bytes, C::kBoxRows)) return BSF_ERR_CUDA;
+  if (!make_map(&map_b, b, static_cast<int64_t>(args.E) * args.N, row_bytes, kBlockW)) return BSF_ERR_CUDA;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<TOK, CPS, MAXE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<TOK, CPS, MAXE, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::kSmem)) != cudaSuccess)
       return BSF_ERR_CUDA;
-    if (CPS > 1 && cudaFuncSetAttribute(grouped_gemm_kernel<TOK, CPS, MAXE>,
+    if (CPS > 1 && cudaFuncSetAttribute(grouped_gemm_kernel<TOK, CPS, MAXE, FMT>,
                                         cudaFuncAttributePreferredSharedMemoryCarveout,
                                         cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return BSF_ERR_CUDA;
@@ -482,9 +562,9 @@ bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int6
   if (max_tiles < grid) grid = max_tiles;
   if (grid <= 0) return BSF_OK;
   if (C::kDependentLaunch)
-    return launch_dependent(grouped_gemm_kernel<TOK, CPS, MAXE>, static_cast<unsigned>(grid), kThreads, C::kSmem, s,
+    return launch_dependent(grouped_gemm_kernel<TOK, CPS, MAXE, FMT>, static_cast<unsigned>(grid), kThreads, C::kSmem, s,
                             map_b, map_a, args);
-  grouped_gemm_kernel<TOK, CPS, MAXE><<<static_cast<unsigned>(grid), kThreads, C::kSmem, s>>>(map_b, map_a, args);
+  grouped_gemm_kernel<TOK, CPS, MAXE, FMT><<<static_cast<unsigned>(grid), kThreads, C::kSmem, s>>>(map_b, map_a, args);
   return launch_status();
 }
 
@@ -509,8 +589,11 @@ bsf_status resolve_b(int flags, const uint8_t** b, const int32_t** sfb) {
 }
 
 bsf_status check_common(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, int64_t m_rows, const uint8_t* b,
-                        const int32_t* sfb, const void* d, int64_t E, int64_t N, int64_t K, int flags) {
+                        const int32_t* sfb, const void* d, int64_t E, int64_t N, int64_t K, int flags,
+                        bool nvfp4 = false) {
   if (E <= 0 || E > kMaxExperts || N <= 0 || K <= 0 || N % 128 || K % 128) return BSF_ERR_INVALID_ARGUMENT;
+  if (nvfp4 && K % 256) return BSF_ERR_INVALID_ARGUMENT;
+  if (nvfp4 && E > kNvfp4MaxE) return BSF_ERR_UNSUPPORTED;
   if (flags & ~(BSF_B_HOST_MAPPED | BSF_DEBUG_WITHHOLD_LOADS)) return BSF_ERR_INVALID_ARGUMENT;
   if (!a || !sfa || !b || !sfb || !d) return BSF_ERR_INVALID_ARGUMENT;
   if (sfa_ld < m_rows || sfa_ld % 4) return BSF_ERR_INVALID_ARGUMENT;
@@ -579,4 +662,55 @@ extern "C" bsf_status bsf_grouped_gemm_masked(const uint8_t* a, const int32_t* s
   }
   const int64_t max_tiles = E * ((max_m + kBigTok - 1) / kBigTok) * (N / 128);
   return launch<kBigTok, 2>(args, a, b, max_tiles, s);
+}
+
+// ---------------------------------------------------------------- NVFP4
+// Same kernel with E2M1 operands and UE4M3 scales per 16 K ("AsymGEMM"
+// README, "FP4 Asymmetric GEMM"; block-scaled MMA kind::mxf4nvf4).
+
+extern "C" bsf_status bsf_grouped_gemm_nvfp4_contig(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld,
+                                                    int64_t m_cap, int a_exp, const uint8_t* b, const int32_t* sfb,
+                                                    const int32_t* b_exp, void* d, const int32_t* seg_start,
+                                                    const int32_t* counts, int64_t E, int64_t N, int64_t K,
+                                                    int flags, bsf_stream_t stream) {
+  if (m_cap <= 0) return m_cap == 0 ? BSF_OK : BSF_ERR_INVALID_ARGUMENT;
+  if (a_exp < -100 || a_exp > 100) return BSF_ERR_INVALID_ARGUMENT;
+  bsf_status st = check_common(a, sfa, sfa_ld, m_cap, b, sfb, d, E, N, K, flags, true);
+  if (st != BSF_OK) return st;
+  if (!seg_start || !counts) return BSF_ERR_INVALID_ARGUMENT;
+  if ((st = resolve_b(flags, &b, &sfb)) != BSF_OK) return st;
+  int* err = device_error_ptr();
+  if (!err) return BSF_ERR_CUDA;
+  GemmArgs args{seg_start, counts, 0, m_cap, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
+                static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
+                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0, a_exp, b_exp};
+  const int64_t max_tiles = (m_cap / 128 + E) * (N / 128);
+  return launch<128, 2, kNvfp4MaxE, kFmtNvfp4>(args, a, b, max_tiles, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" bsf_status bsf_grouped_gemm_nvfp4_masked(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, int a_exp,
+                                                    const uint8_t* b, const int32_t* sfb, const int32_t* b_exp,
+                                                    void* d, const int32_t* masked_m, int64_t E, int64_t max_m,
+                                                    int64_t N, int64_t K, int64_t expected_m, int flags,
+                                                    bsf_stream_t stream) {
+  if (max_m <= 0) return BSF_ERR_INVALID_ARGUMENT;
+  if (a_exp < -100 || a_exp > 100) return BSF_ERR_INVALID_ARGUMENT;
+  const int64_t m_rows = E * max_m;
+  bsf_status st = check_common(a, sfa, sfa_ld, m_rows, b, sfb, d, E, N, K, flags, true);
+  if (st != BSF_OK) return st;
+  if (!masked_m) return BSF_ERR_INVALID_ARGUMENT;
+  if ((st = resolve_b(flags, &b, &sfb)) != BSF_OK) return st;
+  int* err = device_error_ptr();
+  if (!err) return BSF_ERR_CUDA;
+  GemmArgs args{nullptr, masked_m, max_m, m_rows, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
+                static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
+                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0, a_exp, b_exp};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t hint = expected_m > 0 ? expected_m : max_m;
+  if (max_m <= 64 || ((flags & BSF_B_HOST_MAPPED) == 0 && hint <= 32)) {
+    const int64_t max_tiles = E * ((max_m + 63) / 64) * (N / 128);
+    return launch<64, 2, kNvfp4MaxE, kFmtNvfp4>(args, a, b, max_tiles, s);
+  }
+  const int64_t max_tiles = E * ((max_m + 127) / 128) * (N / 128);
+  return launch<128, 2, kNvfp4MaxE, kFmtNvfp4>(args, a, b, max_tiles, s);
 }

@@ -89,9 +89,11 @@ def route_capacity(T: int, kr: int, E: int, layout: int, align_or_max_m: int) ->
 
 
 class RouteBuffers:
-    """Preallocated outputs of ``route`` (reused across steps)."""
+    """Preallocated outputs of ``route`` / ``dispatch`` (reused across steps).  ``fmt`` picks the
+    packed operand: "fp8" (a_packed [m_cap, K], sfa_packed [ceil(K/512), ld]) or "nvfp4"
+    (a_packed [m_cap, K/2], sfa_packed [K/64, ld])."""
 
-    def __init__(self, T, kr, E, layout, align_or_max_m, K=0, device="cuda", scatter=True):
+    def __init__(self, T, kr, E, layout, align_or_max_m, K=0, device="cuda", scatter=True, fmt="fp8"):
         self.T, self.kr, self.E, self.layout, self.align_or_max_m, self.K = T, kr, E, layout, align_or_max_m, K
         self.m_cap = route_capacity(T, kr, E, layout, align_or_max_m)
         i32 = dict(dtype=torch.int32, device=device)
@@ -102,7 +104,11 @@ class RouteBuffers:
         self.m_indices = torch.empty(max(self.m_cap, 1), **i32)
         ws = _lib.load().bsf_route_workspace_bytes(T, kr, E)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
-        if scatter and K:
+        self.fmt = fmt
+        if scatter and K and fmt == "nvfp4":
+            self.a_packed = torch.empty((max(self.m_cap, 1), K // 2), dtype=torch.uint8, device=device)
+            self.sfa_packed = torch.empty((K // 64, sf_ld(self.m_cap)), dtype=torch.int32, device=device)
+        elif scatter and K:
             self.a_packed = torch.empty((max(self.m_cap, 1), K), dtype=torch.uint8, device=device)
             self.sfa_packed = torch.empty((sf_words(K), sf_ld(self.m_cap)), dtype=torch.int32, device=device)
         else:
@@ -193,3 +199,79 @@ def checksum_u64(t, host_mapped=False, out=None, stream=None):
     _lib.check(_lib.load().bsf_checksum_u64(_ptr(t), nbytes, B_HOST_MAPPED if host_mapped else 0, _ptr(out),
                                             _stream(stream)), "checksum_u64")
     return out
+
+
+# ----------------------------------------------------------------------------- NVFP4
+def nvfp4_tensor_exponent(x, groups=1, out=None, stream=None):
+    """Least j per group with max|x| <= 6 * 448 * 2**j; x bf16 split into ``groups`` equal groups."""
+    x = x.contiguous()
+    if out is None:
+        out = torch.empty(groups, dtype=torch.int32, device=x.device)
+    _lib.check(_lib.load().bsf_nvfp4_tensor_exponent(_ptr(x), groups, x.numel() // groups, _ptr(out),
+                                                     _stream(stream)), "nvfp4_tensor_exponent")
+    return out
+
+
+def quantise_act_nvfp4(x, a_exp=0, q=None, sf=None, stream=None):
+    """x bf16 [T, K] -> (q uint8 [T, K/2], sf int32 [K/64, sf_ld(T)])."""
+    T, K = x.shape
+    if q is None:
+        q = torch.empty((T, K // 2), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty((K // 64, sf_ld(T)), dtype=torch.int32, device=x.device)
+    _lib.check(_lib.load().bsf_quantise_act_nvfp4(_ptr(x.contiguous()), T, K, int(a_exp), _ptr(q), _ptr(sf),
+                                                  sf.shape[1], _stream(stream)), "quantise_act_nvfp4")
+    return q, sf
+
+
+def quantise_weight_nvfp4(w, b_exp=None, stream=None):
+    """w bf16 [E, N, K] -> (q uint8 [E, N, K/2], sfb int32 [E, K/64, N], b_exp int32 [E]).
+    Without ``b_exp`` each expert takes its least tensor exponent (``nvfp4_tensor_exponent``)."""
+    E, N, K = w.shape
+    w = w.contiguous()
+    if b_exp is None:
+        b_exp = nvfp4_tensor_exponent(w, groups=E, stream=stream)
+    q = torch.empty((E, N, K // 2), dtype=torch.uint8, device=w.device)
+    sfb = torch.empty((E, K // 64, N), dtype=torch.int32, device=w.device)
+    _lib.check(_lib.load().bsf_quantise_weight_nvfp4(_ptr(w), E, N, K, _ptr(b_exp), _ptr(q), _ptr(sfb),
+                                                     _stream(stream)), "quantise_weight_nvfp4")
+    return q, sfb, b_exp
+
+
+def dispatch_nvfp4(x, topk_ids, E, layout, align_or_max_m, a_exp=0, bufs=None, stream=None):
+    """NVFP4 quantise + route + scatter in one launch (small batches); returns a RouteBuffers."""
+    T, K = x.shape
+    kr = topk_ids.shape[1]
+    if bufs is None:
+        bufs = RouteBuffers(T, kr, E, layout, align_or_max_m, K=K, device=x.device, fmt="nvfp4")
+    _lib.check(_lib.load().bsf_dispatch_nvfp4(
+        _ptr(x.contiguous()), T, K, int(a_exp), _ptr(topk_ids.contiguous()), kr, E, layout, align_or_max_m,
+        _ptr(bufs.counts), _ptr(bufs.seg_start), _ptr(bufs.output_index), _ptr(bufs.token_of_row),
+        _ptr(bufs.m_indices), bufs.m_cap, _ptr(bufs.a_packed), _ptr(bufs.sfa_packed), bufs.sfa_packed.shape[1],
+        _stream(stream)), "dispatch_nvfp4")
+    return bufs
+
+
+def grouped_gemm_nvfp4_contig(a, sfa, a_exp, b, sfb, b_exp, seg_start, counts, d=None, flags=0, stream=None):
+    """a uint8 [m_cap, K/2], b uint8 [E, N, K/2] -> d bf16 [m_cap, N] (segment rows written)."""
+    m_cap, K2 = a.shape
+    E, N, _ = b.shape
+    if d is None:
+        d = torch.empty((m_cap, N), dtype=torch.bfloat16, device=a.device)
+    _lib.check(_lib.load().bsf_grouped_gemm_nvfp4_contig(
+        _ptr(a), _ptr(sfa), sfa.shape[1], m_cap, int(a_exp), _ptr(b), _ptr(sfb), _ptr(b_exp), _ptr(d),
+        _ptr(seg_start), _ptr(counts), E, N, 2 * K2, flags, _stream(stream)), "grouped_gemm_nvfp4_contig")
+    return d
+
+
+def grouped_gemm_nvfp4_masked(a, sfa, a_exp, b, sfb, b_exp, masked_m, max_m, d=None, expected_m=0, flags=0,
+                              stream=None):
+    """a uint8 [E*max_m, K/2], b uint8 [E, N, K/2] -> d bf16 [E*max_m, N]."""
+    K2 = a.shape[-1]
+    E, N, _ = b.shape
+    if d is None:
+        d = torch.empty((E * max_m, N), dtype=torch.bfloat16, device=a.device)
+    _lib.check(_lib.load().bsf_grouped_gemm_nvfp4_masked(
+        _ptr(a), _ptr(sfa), sfa.shape[1], int(a_exp), _ptr(b), _ptr(sfb), _ptr(b_exp), _ptr(d), _ptr(masked_m),
+        E, max_m, N, 2 * K2, expected_m, flags, _stream(stream)), "grouped_gemm_nvfp4_masked")
+    return d

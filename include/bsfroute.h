@@ -277,6 +277,77 @@ bsf_status bsf_combine(const void* y, int64_t y_rows, const int32_t* output_inde
  */
 bsf_status bsf_checksum_u64(const void* p, size_t bytes, int flags, unsigned long long* out, bsf_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * NVFP4 operands ("AsymGEMM" README, "FP4 Asymmetric GEMM": E2M1 data packed
+ * two elements per byte, FP8 E4M3 scale factors; "CuTeDSL bei Perplexity":
+ * one scale per 16 elements).  Formats:
+ *   data   uint8 rows of K/2 bytes; element 2i in the low nibble of byte i;
+ *          E2M1 = sign, 2 exponent bits (bias 1), 1 mantissa bit:
+ *          0, 0.5, 1, 1.5, 2, 3, 4, 6.
+ *   scales int32 words of four unsigned E4M3 bytes, byte i of word w for
+ *          elements 64w + 16i .. 64w + 16i + 15 of its row; MN-major:
+ *          activations [K/64][sf_ld] (sf_ld >= rows, multiple of 4),
+ *          weights [E][K/64][N].
+ *   tensor exponent j (int, |j| <= 100): a power-of-two scale 2**j of the
+ *          whole activation tensor (a_exp) or of each expert's weights
+ *          (b_exp, device int32 [E]); values outside are clamped.
+ * value = e2m1 * scale * 2**j.  Quantisation of a block of 16: amax = max|x|,
+ * scale = E4M3(amax / 6 * 2**-j) (nearest even, saturating at 448),
+ * element = E2M1(x / (scale * 2**j)) (nearest even, saturating at 6), each
+ * step one float32 operation rounded to nearest even; a zero scale stores
+ * zero codes.
+ */
+
+/* bsf_nvfp4_tensor_exponent — for each of `groups` consecutive groups of
+ * `per_group` bf16 values (per_group % 8 == 0): the least j with
+ * max|x| <= 6 * 448 * 2**j (0 for an all-zero group), in [-100, 100], written
+ * to exp_out (device int32 [groups]).  groups <= 65535. */
+bsf_status bsf_nvfp4_tensor_exponent(const void* x, int64_t groups, int64_t per_group, int32_t* exp_out,
+                                     bsf_stream_t stream);
+
+/* bsf_quantise_act_nvfp4 — x bf16 [T, K] (K % 64 == 0) -> q uint8 [T, K/2],
+ * sf int32 [K/64][sf_ld], with tensor exponent a_exp.  16-byte aligned x, q, sf. */
+bsf_status bsf_quantise_act_nvfp4(const void* x, int64_t T, int64_t K, int a_exp, uint8_t* q, int32_t* sf,
+                                  int64_t sf_ld, bsf_stream_t stream);
+
+/* bsf_quantise_weight_nvfp4 — w bf16 [E, N, K] (K % 64 == 0) -> q uint8
+ * [E, N, K/2], sfb int32 [E][K/64][N], expert e with exponent b_exp[e]
+ * (device int32 [E], e.g. from bsf_nvfp4_tensor_exponent with per_group = N*K).
+ * 1 x 16 blocks along K, like the activations. */
+bsf_status bsf_quantise_weight_nvfp4(const void* w, int64_t E, int64_t N, int64_t K, const int32_t* b_exp,
+                                     uint8_t* q, int32_t* sfb, bsf_stream_t stream);
+
+/* bsf_dispatch_nvfp4 — bsf_dispatch for NVFP4 rows: quantise (tensor
+ * exponent a_exp) + route + scatter in one launch for T*kr <=
+ * BSF_DISPATCH_MAX_ASSIGNMENTS and E <= BSF_DISPATCH_MAX_EXPERTS.  a_packed
+ * uint8 [m_cap, K/2], sfa_packed int32 [K/64][sfa_ld]; K % 64 == 0; the bytes
+ * written equal bsf_quantise_act_nvfp4 followed by the row scatter.  Other
+ * arguments, outputs and errors as in bsf_dispatch. */
+bsf_status bsf_dispatch_nvfp4(const void* x, int64_t T, int64_t K, int a_exp, const int32_t* topk_ids, int64_t kr,
+                              int64_t E, int layout, int64_t align_or_max_m, int32_t* counts, int32_t* seg_start,
+                              int32_t* output_index, int32_t* token_of_row, int32_t* m_indices, int64_t m_cap,
+                              uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld, bsf_stream_t stream);
+
+/* bsf_grouped_gemm_nvfp4_contig / _masked — the grouped GEMMs of
+ * bsf_grouped_gemm_contig / _masked on NVFP4 operands:
+ *   D[r, n] = BF16( 2**(a_exp + b_exp[e]) * sum_k e2m1(A[r,k]) sA[r,k/16] e2m1(B_e[n,k]) sB_e[n,k/16] )
+ * FP32 accumulation on the tensor cores (block-scaled MMA, kind::mxf4nvf4),
+ * the power-of-two tensor scale applied exactly to the accumulator, then
+ * round-to-nearest-even to bf16.  a uint8 [rows, K/2], b uint8 [E, N, K/2]
+ * (device, or pinned host with BSF_B_HOST_MAPPED), sfa / sfb as above,
+ * b_exp device int32 [E] or NULL (all 0).  Needs K % 256 == 0, N % 128 == 0,
+ * E <= 256 (else BSF_ERR_UNSUPPORTED), 16-byte aligned a, b, d, sfa, sfb.
+ * Rows, segments, masks, ownership, launch order and errors as in the FP8
+ * calls. */
+bsf_status bsf_grouped_gemm_nvfp4_contig(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, int64_t m_cap,
+                                         int a_exp, const uint8_t* b, const int32_t* sfb, const int32_t* b_exp,
+                                         void* d, const int32_t* seg_start, const int32_t* counts, int64_t E,
+                                         int64_t N, int64_t K, int flags, bsf_stream_t stream);
+bsf_status bsf_grouped_gemm_nvfp4_masked(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, int a_exp,
+                                         const uint8_t* b, const int32_t* sfb, const int32_t* b_exp, void* d,
+                                         const int32_t* masked_m, int64_t E, int64_t max_m, int64_t N, int64_t K,
+                                         int64_t expected_m, int flags, bsf_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

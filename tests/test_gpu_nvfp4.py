@@ -1,0 +1,185 @@
+"""GPU parity of the NVFP4 path against the oracle (oracle/nvfp4.py).
+
+Quantisers, tensor exponents and dispatch are bit-exact; the grouped GEMM is
+within the FP8 GEMM's tolerance (the same FP32 tensor-core accumulation);
+the FP4 GEMM equals the FP8 GEMM on the same values where every sum is exact
+(DeepGEMM article, "精度与吞吐的平衡点": FP4 / FP8 equivalence).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from block_scaled_fp8_route_gb300 import _lib, ops
+from tests.gpu_util import bits16, check_expert_block, i32, require_gpu, u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_gpu()
+
+
+def _x(rows, K, seed, scale_rows=True):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(rows, K, generator=g)
+    if scale_rows:
+        x = x * torch.exp2(torch.randint(-6, 7, (rows, 1), generator=g).float())
+    return x.to(torch.bfloat16)
+
+
+def test_tensor_exponent_matches_oracle(dev):
+    x = _x(64, 512, 1)
+    x[3] = 0
+    x[5, 7] = 3000.0
+    groups = 8
+    got = ops.nvfp4_tensor_exponent(x.to(dev), groups=groups).cpu().numpy()
+    xv = oracle.formats.bf16_bits_to_f64(bits16(x)).reshape(groups, -1)
+    assert np.array_equal(got, oracle.nvfp4.global_exponent(np.abs(xv).max(axis=1)))
+    z = torch.zeros(1024, dtype=torch.bfloat16, device=dev)
+    assert int(ops.nvfp4_tensor_exponent(z)[0]) == 0
+
+
+@pytest.mark.parametrize("a_exp", [0, -4, 6])
+def test_quantise_act_bit_exact(dev, a_exp):
+    T, K = 37, 320                                   # ragged rows, K not a multiple of 256
+    x = _x(T, K, 2 + a_exp)
+    x[0] = 0                                          # all-zero blocks
+    x[1, :16] = torch.tensor([6, 3, -1.5, 0.25, 0.75, -4, 1.25, 1.75, 2.5, 3.5, 5, -0.25, -0.75, 0, 0.5, -6.0])
+    x[2, :16] = 1e-30                                 # scale underflows to 0
+    x[4, 16:32] = 60000.0                             # scale saturates
+    q, sf = ops.quantise_act_nvfp4(x.to(dev), a_exp)
+    torch.cuda.synchronize()
+    q_ref, sf_ref, _ = oracle.nvfp4.quantise_act(bits16(x), a_exp)
+    assert np.array_equal(u8(q), q_ref)
+    assert np.array_equal(sf.cpu().numpy()[:, :T], sf_ref[:, :T])
+
+
+def test_quantise_weight_bit_exact(dev):
+    E, N, K = 3, 256, 512
+    g = torch.Generator().manual_seed(3)
+    w = (torch.randn(E, N, K, generator=g) * 0.02 * torch.tensor([1.0, 30.0, 0.001]).view(E, 1, 1)).to(torch.bfloat16)
+    q, sfb, b_exp = ops.quantise_weight_nvfp4(w.to(dev))
+    torch.cuda.synchronize()
+    wv = oracle.formats.bf16_bits_to_f64(bits16(w))
+    j_ref = oracle.nvfp4.global_exponent(np.abs(wv).reshape(E, -1).max(axis=1))
+    assert np.array_equal(b_exp.cpu().numpy(), j_ref)
+    q_ref, sfb_ref, _ = oracle.nvfp4.quantise_weight(bits16(w), j_ref)
+    assert np.array_equal(u8(q), q_ref)
+    assert np.array_equal(sfb.cpu().numpy(), sfb_ref)
+
+
+def _gemm_operands(rows, E, N, K, seed, dev, a_exp=0):
+    x = _x(rows, K, seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    w = (torch.randn(E, N, K, generator=g) * 0.02).to(torch.bfloat16)
+    aq, asf = ops.quantise_act_nvfp4(x.to(dev), a_exp)
+    bq, sfb, b_exp = ops.quantise_weight_nvfp4(w.to(dev))
+    aq_r, _, asc_r = oracle.nvfp4.quantise_act(bits16(x), a_exp)
+    wv = oracle.formats.bf16_bits_to_f64(bits16(w))
+    j_r = oracle.nvfp4.global_exponent(np.abs(wv).reshape(E, -1).max(axis=1))
+    bq_r, _, bsc_r = oracle.nvfp4.quantise_weight(bits16(w), j_r)
+    return (aq, asf, bq, sfb, b_exp), (aq_r, asc_r, a_exp, bq_r, bsc_r, j_r)
+
+
+def _check(d, ref_ops, seg, counts, what):
+    aq_r, asc_r, aj, bq_r, bsc_r, j_r = ref_ops
+    ref, _ = oracle.nvfp4.grouped_gemm(aq_r, asc_r, aj, bq_r, bsc_r, j_r, seg, counts)
+    dg = bits16(d)
+    for e in range(len(counts)):
+        c, s = int(counts[e]), int(seg[e])
+        if c:
+            check_expert_block(dg[s:s + c], ref[s:s + c], f"{what} expert {e} ({c} rows)")
+
+
+@pytest.mark.parametrize("max_m,expected_m", [(64, 0), (200, 0)])
+def test_masked_gemm(dev, max_m, expected_m):
+    masked = np.minimum(np.array([0, 1, 16, 63, 64, max_m // 2, max_m, 7]), max_m)
+    E, N, K = len(masked), 256, 512
+    ops_, ref_ops = _gemm_operands(E * max_m, E, N, K, 10 + max_m, dev, a_exp=-1)
+    aq, asf, bq, sfb, b_exp = ops_
+    d = torch.full((E * max_m, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    ops.grouped_gemm_nvfp4_masked(aq, asf, -1, bq, sfb, b_exp, torch.as_tensor(masked, dtype=torch.int32,
+                                  device=dev), max_m, d=d, expected_m=expected_m)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    _check(d, ref_ops, np.arange(E + 1) * max_m, masked, f"nvfp4 masked max_m={max_m}")
+
+
+@pytest.mark.parametrize("align", [1, 128])
+def test_contig_gemm_ragged(dev, align):
+    counts = np.array([1, 15, 16, 17, 31, 33, 0, 129, 250, 3])
+    E, N, K = len(counts), 384, 768
+    seg = np.concatenate([[0], np.cumsum((counts + align - 1) // align * align)])
+    rows = int(seg[-1])
+    ops_, ref_ops = _gemm_operands(rows, E, N, K, 20 + align, dev)
+    aq, asf, bq, sfb, b_exp = ops_
+    d = torch.full((rows, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    ops.grouped_gemm_nvfp4_contig(aq, asf, 0, bq, sfb, b_exp, torch.as_tensor(seg, dtype=torch.int32, device=dev),
+                                  torch.as_tensor(counts, dtype=torch.int32, device=dev), d=d)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    _check(d, ref_ops, seg, counts, f"nvfp4 contig align={align}")
+    dv = d.float().cpu().numpy()
+    for e in range(E):
+        assert np.isnan(dv[seg[e] + counts[e]:seg[e + 1]]).all()
+
+
+def test_fp4_gemm_equals_fp8_gemm_on_the_same_values(dev):
+    """Every FP4 scale 1 and every sum exact in FP32: the two block-scaled MMA kinds must agree bit for bit."""
+    rng = np.random.default_rng(11)
+    R, E, N, K = 96, 2, 256, 1024
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    xa = rng.choice(grid, (R, K)) * rng.choice([-1, 1], (R, K))
+    xb = rng.choice(grid, (E, N, K)) * rng.choice([-1, 1], (E, N, K))
+    xa[:, ::16] = 6.0
+    xb[:, :, ::16] = 6.0
+    xa_t = torch.from_numpy(xa).to(torch.bfloat16).to(dev)
+    xb_t = torch.from_numpy(xb).to(torch.bfloat16).to(dev)
+    zeros = torch.zeros(E, dtype=torch.int32, device=dev)
+    aq4, asf4 = ops.quantise_act_nvfp4(xa_t, 0)
+    bq4, sfb4, _ = ops.quantise_weight_nvfp4(xb_t, zeros)
+    counts = torch.tensor([60, 36], dtype=torch.int32, device=dev)
+    seg = torch.tensor([0, 60, 96], dtype=torch.int32, device=dev)
+    d4 = ops.grouped_gemm_nvfp4_contig(aq4, asf4, 0, bq4, sfb4, zeros, seg, counts)
+    # FP8 operands holding the same values (every block's amax is 6: scale 2**-6, codes 64 x value, exact)
+    aq8, asf8 = ops.quantise_act(xa_t)
+    bq8, sf128 = ops.quantise_weight(xb_t)
+    assert torch.all(sf128 == 2.0 ** -6)
+    d8 = ops.grouped_gemm_contig(aq8, asf8, bq8, ops.prepare_weight_sf(sf128, K), seg, counts)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    assert torch.equal(d4.view(torch.int16), d8.view(torch.int16))
+
+
+def test_dispatch_nvfp4_matches_quantise_and_scatter(dev):
+    for name in ("tiny", "decode"):
+        w = W.WORKLOADS[name]
+        ids, _ = W.routing(w)
+        x = W.activations(w)
+        a_or_m = w.max_m if w.layout == W.MASKED else w.align
+        got = ops.dispatch_nvfp4(x.to(dev), ids.to(dev), w.E, w.layout, a_or_m, a_exp=1)
+        torch.cuda.synchronize()
+        assert ops.device_error() == 0
+        q_ref, sf_ref, _ = oracle.nvfp4.quantise_act(bits16(x), 1)
+        r = oracle.route.route(ids.numpy(), w.E, w.layout, align=w.align, max_m=w.max_m)
+        assert np.array_equal(i32(got.output_index), r["output_index"])
+        tok = r["token_of_row"]
+        rows = np.nonzero(tok >= 0)[0]
+        assert np.array_equal(u8(got.a_packed)[rows], q_ref[tok[rows]])
+        assert np.array_equal(got.sfa_packed.cpu().numpy()[:, rows], sf_ref[:, tok[rows]])
+
+
+def test_nvfp4_argument_checks(dev):
+    a = torch.zeros((64, 64), dtype=torch.uint8, device=dev)        # K = 128: not a multiple of 256
+    sfa = torch.zeros((2, 64), dtype=torch.int32, device=dev)
+    b = torch.zeros((1, 128, 64), dtype=torch.uint8, device=dev)
+    sfb = torch.zeros((1, 2, 128), dtype=torch.int32, device=dev)
+    m = torch.zeros(1, dtype=torch.int32, device=dev)
+    with pytest.raises(_lib.BsfError):
+        ops.grouped_gemm_nvfp4_masked(a, sfa, 0, b, sfb, None, m, 64)
+    with pytest.raises(_lib.BsfError):
+        ops.quantise_act_nvfp4(torch.zeros((4, 64), dtype=torch.bfloat16, device=dev), a_exp=101)
