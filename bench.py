@@ -43,6 +43,8 @@ def parse():
                     help="token counts of the host-weight sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fmt", default="fp8", choices=["fp8", "nvfp4"],
+                    help="operand format: FP8 E4M3 with UE8M0 scales, or NVFP4 (E2M1, UE4M3 per 16)")
     ap.add_argument("--no-fused-dispatch", action="store_true",
                     help="quantise + route as separate launches even where the single-launch dispatch applies")
     ap.add_argument("--no-large-m", action="store_true",
@@ -77,29 +79,41 @@ def job_throughput(units_per_step, steps, world, elapsed_ms, scale):
 
 
 # ----------------------------------------------------------------------------- work accounting
-def step_work(w, counts, placed_rows, fused_dispatch=False):
+DTYPES = {"fp8": "e4m3 x e4m3 -> f32 acc -> bf16",
+          "nvfp4": "e2m1 x e2m1 (ue4m3 per 16, 2^j per tensor) -> f32 acc -> bf16"}
+
+
+def operand_bytes(K, fmt):
+    """(data bytes, scale bytes) of one quantised row of K values: FP8 K and one UE8M0 byte per
+    128 packed four to a word; NVFP4 K/2 and one UE4M3 byte per 16."""
+    if fmt == "nvfp4":
+        return K // 2, K // 16
+    return K, ((K // 128 + 3) // 4) * 4
+
+
+def step_work(w, counts, placed_rows, fused_dispatch=False, fmt="fp8"):
     """Algorithmic bytes and GEMM flops of one step (valid rows only; padding excluded).
     With the single-launch dispatch the activations are read once and only the packed
     rows are written; otherwise the token-major quantised copy is written and re-read."""
     T, K, N, E, kr = w.T, w.K, w.N, w.E, w.kr
     R = T * kr
-    nw = (K // 128 + 3) // 4
+    qb, sb = operand_bytes(K, fmt)
     active = [int(c) for c in counts if c > 0]
     rows = sum(active)
     b = {}
     if fused_dispatch:
-        b["dispatch"] = T * K * 2 + R * 4 + R * 4 + placed_rows * 8 + rows * (K + nw * 4)
+        b["dispatch"] = T * K * 2 + R * 4 + R * 4 + placed_rows * 8 + rows * (qb + sb)
     else:
-        b["quantise"] = T * K * 2 + T * K + T * nw * 4
-        b["route"] = R * 4 + R * 4 + placed_rows * 8 + rows * (2 * K + 2 * nw * 4)
-    gemm_bytes = len(active) * (N * K + N * nw * 4) + rows * (K + nw * 4 + N * 2)
+        b["quantise"] = T * K * 2 + T * (qb + sb)
+        b["route"] = R * 4 + R * 4 + placed_rows * 8 + rows * 2 * (qb + sb)
+    gemm_bytes = len(active) * N * (qb + sb) + rows * (qb + sb + N * 2)
     flops = 2.0 * rows * N * K
     b["gemm"] = gemm_bytes
     out_n = N
     if w.K2:
-        nw2 = (w.K2 // 128 + 3) // 4
-        b["quantise2"] = placed_rows * w.K2 * 3 + placed_rows * nw2 * 4
-        b["gemm2"] = len(active) * (w.N2 * w.K2 + w.N2 * nw2 * 4) + rows * (w.K2 + nw2 * 4 + w.N2 * 2)
+        qb2, sb2 = operand_bytes(w.K2, fmt)
+        b["quantise2"] = placed_rows * w.K2 * 2 + placed_rows * (qb2 + sb2)
+        b["gemm2"] = len(active) * w.N2 * (qb2 + sb2) + rows * (qb2 + sb2 + w.N2 * 2)
         flops += 2.0 * rows * w.N2 * w.K2
         out_n = w.N2
     b["combine"] = R * out_n * 2 + T * out_n * 2 + R * 8
@@ -250,10 +264,11 @@ class OracleSample:
     quantise -> route -> scatter -> expert GEMMs -> combine and returns
     (seconds, algorithmic bytes, flops)."""
 
-    def __init__(self, w, n_experts):
+    def __init__(self, w, n_experts, fmt="fp8"):
         import oracle
         self.oracle = oracle
         self.w = w
+        self.fmt = fmt
         x = W.activations(w)
         ids, p = W.routing(w)
         counts = np.bincount(ids.numpy().reshape(-1), minlength=w.E)
@@ -262,31 +277,46 @@ class OracleSample:
         self.xb = x.view(torch.int16).numpy().view(np.uint16)
         self.ids = ids.numpy()
         self.p = p.numpy()
-        self.bq, self.bsf = oracle.quantise.quantise_weight(wt.view(torch.int16).numpy().view(np.uint16))
-        self.desc = (f"oracle (float64 numpy) over the {len(self.experts)} busiest of {w.E} experts; quantise, route, "
-                     f"scatter and combine over the whole batch; first GEMM only")
+        wb = wt.view(torch.int16).numpy().view(np.uint16)
+        if fmt == "nvfp4":
+            wv = oracle.formats.bf16_bits_to_f64(wb)
+            self.bj = oracle.nvfp4.global_exponent(np.abs(wv).reshape(len(self.experts), -1).max(axis=1))
+            self.bq, _, self.bsf = oracle.nvfp4.quantise_weight(wb, self.bj)
+        else:
+            self.bq, self.bsf = oracle.quantise.quantise_weight(wb)
+        self.desc = (f"oracle (float64 numpy, {fmt}) over the {len(self.experts)} busiest of {w.E} experts; quantise, "
+                     f"route, scatter and combine over the whole batch; first GEMM only")
 
     def run(self):
         o, w = self.oracle, self.w
+        fp4 = self.fmt == "nvfp4"
         t0 = time.perf_counter()
-        aq, asf = o.quantise.quantise_act(self.xb)
+        if fp4:
+            aq, _, asf = o.nvfp4.quantise_act(self.xb, 0)
+        else:
+            aq, asf = o.quantise.quantise_act(self.xb)
         r = o.route.route(self.ids, w.E, w.layout, align=w.align, max_m=w.max_m)
         a_rows = o.route.scatter_rows(aq, r["token_of_row"])
-        a_sf = o.route.scatter_rows(asf, r["token_of_row"], pad_value=127)
+        a_sf = o.route.scatter_rows(asf, r["token_of_row"], pad_value=0 if fp4 else 127)
         y = np.zeros((r["rows_used"], w.N), dtype=np.uint16)
         rows = 0
         for i, e in enumerate(self.experts):
             s, c = int(r["seg_start"][e]), int(r["counts"][e])
-            y[s:s + c] = o.gemm.expert_gemm(a_rows[s:s + c], a_sf[s:s + c], self.bq[i], self.bsf[i])
+            if fp4:
+                y[s:s + c], _ = o.nvfp4.grouped_gemm(a_rows[s:s + c], a_sf[s:s + c], 0, self.bq[i:i + 1],
+                                                     self.bsf[i:i + 1], self.bj[i:i + 1], np.array([0, c]),
+                                                     np.array([c]))
+            else:
+                y[s:s + c] = o.gemm.expert_gemm(a_rows[s:s + c], a_sf[s:s + c], self.bq[i], self.bsf[i])
             rows += c
         o.combine.combine(y, r["output_index"], self.p)
         dt = time.perf_counter() - t0
-        nw = (w.K // 128 + 3) // 4
-        byts = len(self.experts) * (w.N * w.K + w.N * nw * 4) + rows * (w.K + nw * 4 + w.N * 2)
+        qb, sb = operand_bytes(w.K, self.fmt)
+        byts = len(self.experts) * w.N * (qb + sb) + rows * (qb + sb + w.N * 2)
         return dt, byts, 2.0 * rows * w.N * w.K
 
 
-def workload_config(w):
+def workload_config(w, fmt="fp8"):
     """The ``config`` object of the JSON line (identical for both arms)."""
     a_or_m = w.max_m if w.layout == W.MASKED else w.align
     ids, _ = W.routing(w)
@@ -299,6 +329,10 @@ def workload_config(w):
            "active_experts": int((counts > 0).sum())}
     if w.K2:
         cfg.update({"K2": w.K2, "N2": w.N2})
+    if fmt != "fp8":
+        cfg["format"] = fmt
+        qb, sb = operand_bytes(w.K, fmt)
+        cfg["l2"] = f"no flush: weights {(w.E * w.N * (qb + sb)) / 1e9:.2f} GB > 129 MB L2, streamed each step"
     return cfg
 
 
@@ -313,7 +347,7 @@ def run_reference(args, w, metric, unit, hib):
     """--impl reference: the oracle as it stands, on the host cores."""
     if int(os.environ.get("RANK", "0")) != 0:
         return
-    sample = OracleSample(w, 2 if w.name in ("decode", "host", "tiny") else 1)
+    sample = OracleSample(w, 2 if w.name in ("decode", "host", "tiny") else 1, fmt=args.fmt)
     for _ in range(args.warmup):
         sample.run()
     tot_t, tot_b, tot_f = 0.0, 0.0, 0.0
@@ -328,7 +362,7 @@ def run_reference(args, w, metric, unit, hib):
         "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
         "higher_is_better": hib, "data": "synthetic", "dtype": "f64",
-        "config": workload_config(w),
+        "config": workload_config(w, args.fmt),
         "cpu_baseline": {"value": value, "unit": unit, "cores": host_cores(), "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -537,7 +571,8 @@ def main():
     a_or_m = w.max_m if w.layout == W.MASKED else w.align
     expected_m = w.T * w.kr // w.E
     path = MoEPath(w.E, w.kr, w.T, w.K, w.N, wt, layout=w.layout, align_or_max_m=a_or_m, w2_bf16=wt2,
-                   device=dev, expected_m=expected_m, fused_dispatch=False if args.no_fused_dispatch else None)
+                   device=dev, expected_m=expected_m, fused_dispatch=False if args.no_fused_dispatch else None,
+                   fmt=args.fmt)
     del wt, wt2
     torch.cuda.empty_cache()
     h2 = W.activations(W.with_tokens(w, path.bufs.m_cap), device=dev, K=w.K2, tag=1) if w.K2 else None
@@ -549,7 +584,7 @@ def main():
     counts = path.bufs.counts.cpu().numpy()
     placed = int(path.bufs.seg_start[-1].item())
     assert ops.device_error() == 0, "device error during setup"
-    bytes_by_kernel, flops = step_work(w, counts, placed, fused_dispatch=path.fused_dispatch)
+    bytes_by_kernel, flops = step_work(w, counts, placed, fused_dispatch=path.fused_dispatch, fmt=args.fmt)
     step_bytes = sum(bytes_by_kernel.values())
 
     for _ in range(args.warmup):
@@ -610,17 +645,20 @@ def main():
 
     if large_m:
         value = job_throughput(flops, args.steps, world, elapsed_ms, 1e12)
-        fp8_peak = 2.0 * pk["bf16_tflops"]           # fp8 dense = 2 x bf16 dense (nominal ratio 4.5 / 2.25)
+        # dense peak of the operand type: the measured bf16 burst x the nominal ratio (fp8 4.5 / 2.25 = 2,
+        # fp4 13.5 / 2.25 = 6)
+        ratio = 6.0 if args.fmt == "nvfp4" else 2.0
+        fp8_peak = ratio * pk["bf16_tflops"]
         gflops = 2.0 * int(counts.sum()) * w.N * w.K
         achieved = gflops / (first_gemm_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                "frac": achieved / fp8_peak, "peak_src": f"2 x bf16 burst ({pk['src']})"}
+                "frac": achieved / fp8_peak, "peak_src": f"{ratio:g} x bf16 burst ({pk['src']})"}
     else:
         value = job_throughput(step_bytes, args.steps, world, elapsed_ms, 1e9)
         achieved = bytes_by_kernel["gemm"] / (first_gemm_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"], "peak_src": pk["src"]}
-    roof["traffic"] = recorded_traffic(w.name)
+    roof["traffic"] = recorded_traffic(w.name if args.fmt == "fp8" else f"{w.name}_{args.fmt}")
     roof["kernel"] = "grouped_gemm_kernel"
     roof["algorithmic_per_launch"] = bytes_by_kernel["gemm"] if not large_m else 2.0 * int(counts.sum()) * w.N * w.K
     roof["launch_ms"] = first_gemm_ms
@@ -659,7 +697,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample = OracleSample(w, 16 if w.name == "decode" else 3)
+        sample = OracleSample(w, 16 if w.name == "decode" else 3, fmt=args.fmt)
         tot_t = tot_b = tot_f = 0.0
         reps = 0
         while tot_t < 10.0 and reps < 50:          # about 10 s of oracle time
@@ -680,16 +718,16 @@ def main():
         torch.cuda.empty_cache()
 
     large_m = None
-    if rank == 0 and world == 1 and w.name == "decode" and not args.no_large_m:
+    if rank == 0 and world == 1 and w.name == "decode" and args.fmt == "fp8" and not args.no_large_m:
         del path
         torch.cuda.empty_cache()
         large_m = large_m_gemms(dev, pk)
     if rank == 0:
-        cfg = workload_config(w)
+        cfg = workload_config(w, args.fmt)
         line = {
             "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 acc -> bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": DTYPES[args.fmt],
             "data": "synthetic", "config": cfg,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
             "gpu_launches": launches_per_step * args.steps,

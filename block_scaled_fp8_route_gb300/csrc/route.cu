@@ -207,13 +207,15 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const int32_
 constexpr int kFillRows = 32;   // packed rows per CTA in route_fill
 
 // Per packed row r < seg_start[E]: mark padding rows (token -1), write
-// m_indices, and copy a routed row's FP8 data and SF words.
+// m_indices, and copy a routed row's data (row_bytes, FP8 or NVFP4) and its
+// n_words SF words.
 __global__ void __launch_bounds__(kThreads) route_fill_kernel(int E, int64_t m_cap, const int32_t* __restrict__ counts,
                                                               const int32_t* __restrict__ seg_start,
                                                               int32_t* __restrict__ token_of_row,
                                                               int32_t* __restrict__ m_indices,
                                                               const uint8_t* __restrict__ q,
-                                                              const int32_t* __restrict__ sf, int64_t sf_ld, int64_t K,
+                                                              const int32_t* __restrict__ sf, int64_t sf_ld,
+                                                              int64_t row_bytes, int64_t n_words,
                                                               uint8_t* __restrict__ a_packed,
                                                               int32_t* __restrict__ sfa_packed, int64_t sfa_ld) {
   pdl_launch_dependents();     // a dependent GEMM may be scheduled now; it waits for completion
@@ -247,7 +249,6 @@ __global__ void __launch_bounds__(kThreads) route_fill_kernel(int E, int64_t m_c
   // SF words of routed rows: thread (word i, row) with consecutive rows -> coalesced stores.
   // Padding rows keep whatever the buffer held: "GEMM 执行方式" §4.6 leaves them
   // uninitialised, and no computed output row depends on them.
-  const int64_t n_words = (K + 511) / 512;
   for (int64_t j = threadIdx.x; j < n_words * kFillRows; j += kThreads) {
     const int64_t i = j / kFillRows;
     const int rl = static_cast<int>(j % kFillRows);
@@ -255,14 +256,14 @@ __global__ void __launch_bounds__(kThreads) route_fill_kernel(int E, int64_t m_c
     if (t < 0) continue;
     sfa_packed[i * sfa_ld + row0 + rl] = sf[i * sf_ld + t];
   }
-  // FP8 rows: one warp per routed row, 16-byte vectors
+  // data rows: one warp per routed row, 16-byte vectors
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t nvec = K / 16;
+  const int64_t nvec = row_bytes / 16;
   for (int rl = warp; rl < kFillRows; rl += kWarps) {
     const int t = tok[rl];
     if (t < 0) continue;
-    uint4* dst = reinterpret_cast<uint4*>(a_packed + (row0 + rl) * K);
-    const uint4* src = reinterpret_cast<const uint4*>(q + static_cast<int64_t>(t) * K);
+    uint4* dst = reinterpret_cast<uint4*>(a_packed + (row0 + rl) * row_bytes);
+    const uint4* src = reinterpret_cast<const uint4*>(q + static_cast<int64_t>(t) * row_bytes);
     for (int64_t v = lane; v < nvec; v += 32) dst[v] = __ldg(src + v);
   }
 }
@@ -279,11 +280,15 @@ extern "C" size_t bsf_route_workspace_bytes(int64_t T, int64_t kr, int64_t E) {
   return static_cast<size_t>((nblk > 0 ? nblk : 1) * E * sizeof(int32_t));
 }
 
-extern "C" bsf_status bsf_route(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout,
-                                int64_t align_or_max_m, int32_t* counts, int32_t* seg_start, int32_t* output_index,
-                                int32_t* token_of_row, int32_t* m_indices, int64_t m_cap, const uint8_t* q,
-                                const int32_t* sf, int64_t sf_ld, int64_t K, uint8_t* a_packed, int32_t* sfa_packed,
-                                int64_t sfa_ld, void* workspace, size_t workspace_bytes, bsf_stream_t stream) {
+namespace bsf {
+namespace {
+
+// bsf_route / bsf_route_nvfp4: nvfp4 selects the scatter's row format.
+bsf_status route_impl(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout, int64_t align_or_max_m,
+                      int32_t* counts, int32_t* seg_start, int32_t* output_index, int32_t* token_of_row,
+                      int32_t* m_indices, int64_t m_cap, const uint8_t* q, const int32_t* sf, int64_t sf_ld,
+                      int64_t K, bool nvfp4, uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld,
+                      void* workspace, size_t workspace_bytes, bsf_stream_t stream) {
   if (T < 0 || kr <= 0 || E <= 0 || E > kMaxExperts) return BSF_ERR_INVALID_ARGUMENT;
   if (layout != BSF_LAYOUT_CONTIGUOUS && layout != BSF_LAYOUT_MASKED) return BSF_ERR_INVALID_ARGUMENT;
   if (align_or_max_m < 1) return BSF_ERR_INVALID_ARGUMENT;
@@ -294,7 +299,7 @@ extern "C" bsf_status bsf_route(const int32_t* topk_ids, int64_t T, int64_t kr, 
   if (R > INT32_MAX) return BSF_ERR_UNSUPPORTED;
   if (workspace_bytes < bsf_route_workspace_bytes(T, kr, E) || !workspace) return BSF_ERR_INVALID_ARGUMENT;
   if (q) {
-    if (!sf || !a_packed || !sfa_packed || K <= 0 || K % 128) return BSF_ERR_INVALID_ARGUMENT;
+    if (!sf || !a_packed || !sfa_packed || K <= 0 || K % (nvfp4 ? 64 : 128)) return BSF_ERR_INVALID_ARGUMENT;
     if (sf_ld < T || sf_ld % 4 || sfa_ld < m_cap || sfa_ld % 4) return BSF_ERR_INVALID_ARGUMENT;
     if (!aligned16(q) || !aligned16(a_packed) || !aligned16(sf) || !aligned16(sfa_packed)) return BSF_ERR_MISALIGNED;
   }
@@ -322,9 +327,34 @@ extern "C" bsf_status bsf_route(const int32_t* topk_ids, int64_t T, int64_t kr, 
   const int64_t fill_blocks = (m_cap + kFillRows - 1) / kFillRows;
   if (fill_blocks > 0) {
     route_fill_kernel<<<static_cast<unsigned>(fill_blocks), kThreads, 0, s>>>(
-        e32, m_cap, counts, seg_start, token_of_row, m_indices, q, sf, sf_ld, K, a_packed, sfa_packed, sfa_ld);
+        e32, m_cap, counts, seg_start, token_of_row, m_indices, q, sf, sf_ld, nvfp4 ? K / 2 : K,
+        nvfp4 ? K / 64 : (K + 511) / 512, a_packed, sfa_packed, sfa_ld);
   }
   return launch_status();
+}
+
+}  // namespace
+}  // namespace bsf
+
+extern "C" bsf_status bsf_route(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout,
+                                int64_t align_or_max_m, int32_t* counts, int32_t* seg_start, int32_t* output_index,
+                                int32_t* token_of_row, int32_t* m_indices, int64_t m_cap, const uint8_t* q,
+                                const int32_t* sf, int64_t sf_ld, int64_t K, uint8_t* a_packed, int32_t* sfa_packed,
+                                int64_t sfa_ld, void* workspace, size_t workspace_bytes, bsf_stream_t stream) {
+  return route_impl(topk_ids, T, kr, E, layout, align_or_max_m, counts, seg_start, output_index, token_of_row,
+                    m_indices, m_cap, q, sf, sf_ld, K, false, a_packed, sfa_packed, sfa_ld, workspace,
+                    workspace_bytes, stream);
+}
+
+extern "C" bsf_status bsf_route_nvfp4(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout,
+                                      int64_t align_or_max_m, int32_t* counts, int32_t* seg_start,
+                                      int32_t* output_index, int32_t* token_of_row, int32_t* m_indices,
+                                      int64_t m_cap, const uint8_t* q, const int32_t* sf, int64_t sf_ld, int64_t K,
+                                      uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld, void* workspace,
+                                      size_t workspace_bytes, bsf_stream_t stream) {
+  return route_impl(topk_ids, T, kr, E, layout, align_or_max_m, counts, seg_start, output_index, token_of_row,
+                    m_indices, m_cap, q, sf, sf_ld, K, true, a_packed, sfa_packed, sfa_ld, workspace,
+                    workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

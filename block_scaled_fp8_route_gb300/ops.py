@@ -115,14 +115,16 @@ class RouteBuffers:
             self.a_packed = self.sfa_packed = None
 
 
-def route(topk_ids, E, layout, align_or_max_m, q=None, sf=None, bufs=None, stream=None):
-    """Routing + optional scatter; returns a RouteBuffers holding every output."""
+def route(topk_ids, E, layout, align_or_max_m, q=None, sf=None, bufs=None, stream=None, fmt="fp8"):
+    """Routing + optional scatter of quantised rows (``fmt`` "fp8" or "nvfp4"); returns a RouteBuffers."""
     T, kr = topk_ids.shape
-    K = q.shape[1] if q is not None else 0
+    K = (q.shape[1] * (2 if fmt == "nvfp4" else 1)) if q is not None else 0
     if bufs is None:
-        bufs = RouteBuffers(T, kr, E, layout, align_or_max_m, K=K, device=topk_ids.device, scatter=q is not None)
+        bufs = RouteBuffers(T, kr, E, layout, align_or_max_m, K=K, device=topk_ids.device, scatter=q is not None,
+                            fmt=fmt)
     lib = _lib.load()
-    _lib.check(lib.bsf_route(
+    fn = lib.bsf_route_nvfp4 if fmt == "nvfp4" else lib.bsf_route
+    _lib.check(fn(
         _ptr(topk_ids.contiguous()), T, kr, E, layout, align_or_max_m,
         _ptr(bufs.counts), _ptr(bufs.seg_start), _ptr(bufs.output_index), _ptr(bufs.token_of_row),
         _ptr(bufs.m_indices), bufs.m_cap,

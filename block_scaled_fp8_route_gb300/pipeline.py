@@ -6,7 +6,8 @@
 with an optional second grouped GEMM (the down projection, K2 x N2) on a
 separately supplied packed bf16 input that shares the routing; then the
 combine reads the second GEMM's output.  Weights are quantised once at
-construction (``quantise_weight`` + ``prepare_weight_sf``).  Every step is a
+construction (``quantise_weight`` + ``prepare_weight_sf``, or
+``quantise_weight_nvfp4`` with ``fmt="nvfp4"``).  Every step is a
 ``libbsfroute.so`` call; this class only owns buffers and orders the calls on
 one stream.
 """
@@ -17,35 +18,53 @@ from . import ops
 
 
 class MoEPath:
+    """``fmt`` = "fp8" (E4M3, UE8M0 per 1 x 128 / 128 x 128) or "nvfp4" (E2M1, UE4M3 per 1 x 16, a
+    power-of-two tensor exponent per expert for the weights and ``a_exp`` for the activations)."""
+
     def __init__(self, E, kr, T, K, N, w_bf16, layout=ops.CONTIGUOUS, align_or_max_m=1, w2_bf16=None,
-                 device="cuda", weights_on_host=False, expected_m=0, fused_dispatch=None):
+                 device="cuda", weights_on_host=False, expected_m=0, fused_dispatch=None, fmt="fp8", a_exp=0):
         self.E, self.kr, self.T, self.K, self.N = E, kr, T, K, N
         self.layout, self.align_or_max_m = layout, align_or_max_m
         self.expected_m = expected_m
+        self.fmt, self.a_exp = fmt, a_exp
         self.flags = ops.B_HOST_MAPPED if weights_on_host else 0
-        self.wq, sf128 = ops.quantise_weight(w_bf16.to(device))
-        self.sfb = ops.prepare_weight_sf(sf128, K)
+        self.wq, self.sfb, self.b_exp = self._weights(w_bf16.to(device), K)
         if weights_on_host:
             self.wq = self.wq.cpu().pin_memory()
             self.sfb = self.sfb.cpu().pin_memory()
         self.two_gemms = w2_bf16 is not None
         if self.two_gemms:
             _, self.N2, self.K2 = w2_bf16.shape
-            self.w2q, sf2 = ops.quantise_weight(w2_bf16.to(device))
-            self.sfb2 = ops.prepare_weight_sf(sf2, self.K2)
-        self.bufs = ops.RouteBuffers(T, kr, E, layout, align_or_max_m, K=K, device=device)
+            self.w2q, self.sfb2, self.b2_exp = self._weights(w2_bf16.to(device), self.K2)
+        self.bufs = ops.RouteBuffers(T, kr, E, layout, align_or_max_m, K=K, device=device, fmt=fmt)
         self.fused_dispatch = ops.dispatch_supported(T, kr, E) if fused_dispatch is None else fused_dispatch
         m = self.bufs.m_cap
-        self.q = torch.empty((T, K), dtype=torch.uint8, device=device)
-        self.sf = torch.empty((ops.sf_words(K), ops.sf_ld(T)), dtype=torch.int32, device=device)
+        self.q, self.sf = self._act_buffers(T, K, device)
         self.y = torch.empty((max(m, 1), N), dtype=torch.bfloat16, device=device)
         if self.two_gemms:
-            self.q2 = torch.empty((max(m, 1), self.K2), dtype=torch.uint8, device=device)
-            self.sf2 = torch.empty((ops.sf_words(self.K2), ops.sf_ld(m)), dtype=torch.int32, device=device)
+            self.q2, self.sf2 = self._act_buffers(max(m, 1), self.K2, device)
             self.y2 = torch.empty((max(m, 1), self.N2), dtype=torch.bfloat16, device=device)
             self.z = torch.empty((T, self.N2), dtype=torch.bfloat16, device=device)
         else:
             self.z = torch.empty((T, N), dtype=torch.bfloat16, device=device)
+
+    def _weights(self, w, K):
+        if self.fmt == "nvfp4":
+            return ops.quantise_weight_nvfp4(w)
+        wq, sf128 = ops.quantise_weight(w)
+        return wq, ops.prepare_weight_sf(sf128, K), None
+
+    def _act_buffers(self, rows, K, device):
+        if self.fmt == "nvfp4":
+            return (torch.empty((rows, K // 2), dtype=torch.uint8, device=device),
+                    torch.empty((K // 64, ops.sf_ld(rows)), dtype=torch.int32, device=device))
+        return (torch.empty((rows, K), dtype=torch.uint8, device=device),
+                torch.empty((ops.sf_words(K), ops.sf_ld(rows)), dtype=torch.int32, device=device))
+
+    def _quantise(self, x, q, sf):
+        if self.fmt == "nvfp4":
+            return ops.quantise_act_nvfp4(x, self.a_exp, q=q, sf=sf)
+        return ops.quantise_act(x, q=q, sf=sf)
 
     def launches_per_step(self):
         """Kernel launches one ``step`` makes (all of them this library's kernels)."""
@@ -59,8 +78,15 @@ class MoEPath:
             n += 2                                                 # quantise of h2 + second GEMM
         return n + 1                                               # combine
 
-    def gemm(self, a, sfa, wq, sfb, d):
+    def gemm(self, a, sfa, wq, sfb, d, b_exp=None):
         b = self.bufs
+        if self.fmt == "nvfp4":
+            if self.layout == ops.MASKED:
+                return ops.grouped_gemm_nvfp4_masked(a, sfa, self.a_exp, wq, sfb, b_exp, b.counts,
+                                                     self.align_or_max_m, d=d, expected_m=self.expected_m,
+                                                     flags=self.flags)
+            return ops.grouped_gemm_nvfp4_contig(a, sfa, self.a_exp, wq, sfb, b_exp, b.seg_start, b.counts, d=d,
+                                                 flags=self.flags)
         if self.layout == ops.MASKED:
             return ops.grouped_gemm_masked(a, sfa, wq, sfb, b.counts, self.align_or_max_m, d=d,
                                            expected_m=self.expected_m, flags=self.flags)
@@ -70,16 +96,20 @@ class MoEPath:
         """Run the whole path; ``h2`` is the packed bf16 [m_cap, K2] input of the second GEMM;
         the combined output goes to ``z`` (default: this object's output buffer).  Small batches
         quantise, route and scatter in one launch (``dispatch``)."""
-        if self.fused_dispatch:
+        if self.fused_dispatch and self.fmt == "nvfp4":
+            ops.dispatch_nvfp4(x, topk_ids, self.E, self.layout, self.align_or_max_m, a_exp=self.a_exp,
+                               bufs=self.bufs)
+        elif self.fused_dispatch:
             ops.dispatch(x, topk_ids, self.E, self.layout, self.align_or_max_m, bufs=self.bufs)
         else:
-            ops.quantise_act(x, q=self.q, sf=self.sf)
-            ops.route(topk_ids, self.E, self.layout, self.align_or_max_m, q=self.q, sf=self.sf, bufs=self.bufs)
-        self.gemm(self.bufs.a_packed, self.bufs.sfa_packed, self.wq, self.sfb, self.y)
+            self._quantise(x, self.q, self.sf)
+            ops.route(topk_ids, self.E, self.layout, self.align_or_max_m, q=self.q, sf=self.sf, bufs=self.bufs,
+                      fmt=self.fmt)
+        self.gemm(self.bufs.a_packed, self.bufs.sfa_packed, self.wq, self.sfb, self.y, self.b_exp)
         out = self.y
         if self.two_gemms:
-            ops.quantise_act(h2, q=self.q2, sf=self.sf2)
-            self.gemm(self.q2, self.sf2, self.w2q, self.sfb2, self.y2)
+            self._quantise(h2, self.q2, self.sf2)
+            self.gemm(self.q2, self.sf2, self.w2q, self.sfb2, self.y2, self.b2_exp)
             out = self.y2
         z = self.z if z is None else z
         ops.combine(out, self.bufs.output_index, topk_weights, z=z)

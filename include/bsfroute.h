@@ -328,6 +328,16 @@ bsf_status bsf_dispatch_nvfp4(const void* x, int64_t T, int64_t K, int a_exp, co
                               int32_t* output_index, int32_t* token_of_row, int32_t* m_indices, int64_t m_cap,
                               uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld, bsf_stream_t stream);
 
+/* bsf_route_nvfp4 — bsf_route whose scatter copies NVFP4 rows: q uint8 [T, K/2]
+ * and sf int32 [K/64][sf_ld] (from bsf_quantise_act_nvfp4) into a_packed uint8
+ * [m_cap, K/2] and sfa_packed int32 [K/64][sfa_ld]; K % 64 == 0.  Routing
+ * outputs, workspace and errors as in bsf_route. */
+bsf_status bsf_route_nvfp4(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout,
+                           int64_t align_or_max_m, int32_t* counts, int32_t* seg_start, int32_t* output_index,
+                           int32_t* token_of_row, int32_t* m_indices, int64_t m_cap, const uint8_t* q,
+                           const int32_t* sf, int64_t sf_ld, int64_t K, uint8_t* a_packed, int32_t* sfa_packed,
+                           int64_t sfa_ld, void* workspace, size_t workspace_bytes, bsf_stream_t stream);
+
 /* bsf_grouped_gemm_nvfp4_contig / _masked — the grouped GEMMs of
  * bsf_grouped_gemm_contig / _masked on NVFP4 operands:
  *   D[r, n] = BF16( 2**(a_exp + b_exp[e]) * sum_k e2m1(A[r,k]) sA[r,k/16] e2m1(B_e[n,k]) sB_e[n,k/16] )

@@ -183,3 +183,74 @@ def test_nvfp4_argument_checks(dev):
         ops.grouped_gemm_nvfp4_masked(a, sfa, 0, b, sfb, None, m, 64)
     with pytest.raises(_lib.BsfError):
         ops.quantise_act_nvfp4(torch.zeros((4, 64), dtype=torch.bfloat16, device=dev), a_exp=101)
+
+
+def _exp_of(wt):
+    wv = oracle.formats.bf16_bits_to_f64(bits16(wt))
+    return oracle.nvfp4.global_exponent(np.abs(wv).reshape(wv.shape[0], -1).max(axis=1))
+
+
+def test_decode_full_size_sampled(dev):
+    """The decode workload's grouped GEMM at full size (128 experts, K 4096, N 3072), 14 sampled experts."""
+    w = W.WORKLOADS["decode"]
+    ids, _ = W.routing(w)
+    r = oracle.route.route(ids.numpy(), w.E, w.layout, max_m=w.max_m)
+    bufs = ops.route(ids.to(dev), w.E, w.layout, w.max_m)
+    x = W.activations(W.with_tokens(w, bufs.m_cap), device=dev)
+    aq, asf = ops.quantise_act_nvfp4(x, 0)
+    wt = W.weights(w, device=dev)
+    bq, sfb, b_exp = ops.quantise_weight_nvfp4(wt)
+    d = ops.grouped_gemm_nvfp4_masked(aq, asf, 0, bq, sfb, b_exp, bufs.counts, w.max_m, expected_m=8)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    counts = r["counts"]
+    active = [e for e in range(w.E) if counts[e] > 0]
+    by_size = sorted(active, key=lambda e: counts[e])
+    pick = sorted({by_size[0], by_size[-1]} | set(np.random.default_rng(0).choice(active, 12, replace=False).tolist()))
+    dg = bits16(d)
+    for e in pick:
+        s, c = e * w.max_m, int(counts[e])
+        aq_r, _, asc_r = oracle.nvfp4.quantise_act(bits16(x[s:s + c]), 0)
+        assert np.array_equal(u8(aq[s:s + c]), aq_r)
+        j = _exp_of(wt[e:e + 1])
+        assert int(b_exp[e]) == int(j[0])
+        bq_r, _, bsc_r = oracle.nvfp4.quantise_weight(bits16(wt[e:e + 1]), j)
+        ref, _ = oracle.nvfp4.grouped_gemm(aq_r, asc_r, 0, bq_r, bsc_r, j, np.array([0, c]), np.array([c]))
+        check_expert_block(dg[s:s + c], ref[:c], f"nvfp4 decode expert {e} ({c} rows)")
+
+
+DECODE_SMALL = W.Workload("decode_small", T=128, kr=8, E=128, K=1024, N=256, layout=W.MASKED, max_m=64, seed=1001)
+
+
+@pytest.mark.parametrize("name,fused", [("tiny", True), ("tiny_a128", False), ("decode_small", True),
+                                        ("decode_small", False)])
+def test_nvfp4_end_to_end(dev, name, fused):
+    from block_scaled_fp8_route_gb300 import MoEPath
+    from tests.gpu_util import check_combined, expert_row_rms
+    w = DECODE_SMALL if name == "decode_small" else W.WORKLOADS[name]
+    x, wt = W.activations(w), W.weights(w)
+    ids, p = W.routing(w)
+    a_or_m = w.max_m if w.layout == W.MASKED else w.align
+    path = MoEPath(w.E, w.kr, w.T, w.K, w.N, wt, layout=w.layout, align_or_max_m=a_or_m, device=dev,
+                   expected_m=w.T * w.kr // w.E, fused_dispatch=fused, fmt="nvfp4", a_exp=-1)
+    z = path.step(x.to(dev), ids.to(dev), p.to(dev))
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    # oracle: quantise, route, scatter, NVFP4 grouped GEMM, combine
+    aq, _, asc = oracle.nvfp4.quantise_act(bits16(x), -1)
+    j = _exp_of(wt)
+    bq, _, bsc = oracle.nvfp4.quantise_weight(bits16(wt), j)
+    r = oracle.route.route(ids.numpy(), w.E, w.layout, align=w.align if w.layout == W.CONTIGUOUS else 1,
+                           max_m=a_or_m if w.layout == W.MASKED else 0)
+    a_rows = oracle.route.scatter_rows(aq, r["token_of_row"])
+    a_sc = oracle.route.scatter_rows(asc, r["token_of_row"])
+    y_ref, _ = oracle.nvfp4.grouped_gemm(a_rows, a_sc, -1, bq, bsc, j, r["seg_start"], r["counts"])
+    z_ref = oracle.combine.combine(y_ref, r["output_index"], p.numpy())
+    assert np.array_equal(i32(path.bufs.output_index), r["output_index"])
+    yg = bits16(path.y)
+    for e in range(w.E):
+        s, c = int(r["seg_start"][e]), int(r["counts"][e])
+        if c:
+            check_expert_block(yg[s:s + c], y_ref[s:s + c], f"nvfp4 {name} expert {e}")
+    rms = expert_row_rms(y_ref, r["seg_start"], r["counts"])
+    check_combined(bits16(z), z_ref, y_ref, r["output_index"], p.numpy(), rms, f"nvfp4 {name} combined")
