@@ -17,7 +17,8 @@ Sources (page title, section):
   UE8M0 packing), "补偿机制三" (MN-major packed SF layout), "精度与吞吐的平衡点"
   (calc_diff tolerance, repeat-run determinism).
 * "AsymGEMM" README, "Token Layout Protocols" (contiguous and masked layouts),
-  "FP4 Asymmetric GEMM" (NVFP4 operands, ``oracle/nvfp4.py``).
+  "FP4 Asymmetric GEMM" (NVFP4 operands, ``oracle/nvfp4.py``), "BF16 Asymmetric
+  GEMM" (``oracle/bf16.py``).
 * "CuTeDSL bei Perplexity", Blackwell support (16-element absolute maximum
   of the NVFP4 quantiser).
 
@@ -27,4 +28,4 @@ values the pages print, closed forms, library routines or brute force, except
 the GPU-internal FP32 accumulation order, which is outside the oracle.
 """
 
-from . import formats, quantise, route, gemm, combine, checks, nvfp4  # noqa: F401
+from . import formats, quantise, route, gemm, combine, checks, nvfp4, bf16  # noqa: F401

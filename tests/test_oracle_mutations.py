@@ -133,3 +133,15 @@ def test_global_exponent_off_by_one_is_caught(monkeypatch):
     orig = nvfp4.global_exponent
     monkeypatch.setattr(nvfp4, "global_exponent", lambda a: orig(a) + 1)
     _fails(pin_nvfp4.test_global_exponent_is_least)
+
+
+# ---------------------------------------------------------------- BF16
+from oracle import bf16 as bf16_oracle  # noqa: E402
+from tests import test_oracle_bf16 as pin_bf16  # noqa: E402
+
+
+def test_bf16_wrong_expert_weights_are_caught(monkeypatch):
+    orig = bf16_oracle.grouped_gemm
+    monkeypatch.setattr(bf16_oracle, "grouped_gemm",
+                        lambda a, b, seg, counts: orig(a, np.roll(b, 1, axis=0), seg, counts))
+    _fails(pin_bf16.test_exact_rational_brute_force)
