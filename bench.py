@@ -43,8 +43,8 @@ def parse():
                     help="token counts of the host-weight sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--fmt", default="fp8", choices=["fp8", "nvfp4"],
-                    help="operand format: FP8 E4M3 with UE8M0 scales, or NVFP4 (E2M1, UE4M3 per 16)")
+    ap.add_argument("--fmt", default="fp8", choices=["fp8", "nvfp4", "bf16"],
+                    help="operand format: FP8 E4M3 with UE8M0 scales, NVFP4 (E2M1, UE4M3 per 16) or BF16")
     ap.add_argument("--no-fused-dispatch", action="store_true",
                     help="quantise + route as separate launches even where the single-launch dispatch applies")
     ap.add_argument("--no-large-m", action="store_true",
@@ -80,7 +80,8 @@ def job_throughput(units_per_step, steps, world, elapsed_ms, scale):
 
 # ----------------------------------------------------------------------------- work accounting
 DTYPES = {"fp8": "e4m3 x e4m3 -> f32 acc -> bf16",
-          "nvfp4": "e2m1 x e2m1 (ue4m3 per 16, 2^j per tensor) -> f32 acc -> bf16"}
+          "nvfp4": "e2m1 x e2m1 (ue4m3 per 16, 2^j per tensor) -> f32 acc -> bf16",
+          "bf16": "bf16 x bf16 -> f32 acc -> bf16"}
 
 
 def operand_bytes(K, fmt):
@@ -88,6 +89,8 @@ def operand_bytes(K, fmt):
     128 packed four to a word; NVFP4 K/2 and one UE4M3 byte per 16."""
     if fmt == "nvfp4":
         return K // 2, K // 16
+    if fmt == "bf16":
+        return 2 * K, 0
     return K, ((K // 128 + 3) // 4) * 4
 
 
@@ -101,7 +104,9 @@ def step_work(w, counts, placed_rows, fused_dispatch=False, fmt="fp8"):
     active = [int(c) for c in counts if c > 0]
     rows = sum(active)
     b = {}
-    if fused_dispatch:
+    if fmt == "bf16":
+        b["route"] = R * 4 + R * 4 + placed_rows * 8 + rows * 2 * qb       # indices + bf16 row copy
+    elif fused_dispatch:
         b["dispatch"] = T * K * 2 + R * 4 + R * 4 + placed_rows * 8 + rows * (qb + sb)
     else:
         b["quantise"] = T * K * 2 + T * (qb + sb)
@@ -112,7 +117,8 @@ def step_work(w, counts, placed_rows, fused_dispatch=False, fmt="fp8"):
     out_n = N
     if w.K2:
         qb2, sb2 = operand_bytes(w.K2, fmt)
-        b["quantise2"] = placed_rows * w.K2 * 2 + placed_rows * (qb2 + sb2)
+        if fmt != "bf16":
+            b["quantise2"] = placed_rows * w.K2 * 2 + placed_rows * (qb2 + sb2)
         b["gemm2"] = len(active) * w.N2 * (qb2 + sb2) + rows * (qb2 + sb2 + w.N2 * 2)
         flops += 2.0 * rows * w.N2 * w.K2
         out_n = w.N2
@@ -278,7 +284,9 @@ class OracleSample:
         self.ids = ids.numpy()
         self.p = p.numpy()
         wb = wt.view(torch.int16).numpy().view(np.uint16)
-        if fmt == "nvfp4":
+        if fmt == "bf16":
+            self.bq, self.bsf = wb, None
+        elif fmt == "nvfp4":
             wv = oracle.formats.bf16_bits_to_f64(wb)
             self.bj = oracle.nvfp4.global_exponent(np.abs(wv).reshape(len(self.experts), -1).max(axis=1))
             self.bq, _, self.bsf = oracle.nvfp4.quantise_weight(wb, self.bj)
@@ -289,9 +297,11 @@ class OracleSample:
 
     def run(self):
         o, w = self.oracle, self.w
-        fp4 = self.fmt == "nvfp4"
+        fp4, bf = self.fmt == "nvfp4", self.fmt == "bf16"
         t0 = time.perf_counter()
-        if fp4:
+        if bf:
+            aq, asf = self.xb, np.zeros((self.xb.shape[0], 1), dtype=np.uint8)
+        elif fp4:
             aq, _, asf = o.nvfp4.quantise_act(self.xb, 0)
         else:
             aq, asf = o.quantise.quantise_act(self.xb)
@@ -302,7 +312,10 @@ class OracleSample:
         rows = 0
         for i, e in enumerate(self.experts):
             s, c = int(r["seg_start"][e]), int(r["counts"][e])
-            if fp4:
+            if bf:
+                y[s:s + c], _ = o.bf16.grouped_gemm(a_rows[s:s + c], self.bq[i:i + 1], np.array([0, c]),
+                                                    np.array([c]))
+            elif fp4:
                 y[s:s + c], _ = o.nvfp4.grouped_gemm(a_rows[s:s + c], a_sf[s:s + c], 0, self.bq[i:i + 1],
                                                      self.bsf[i:i + 1], self.bj[i:i + 1], np.array([0, c]),
                                                      np.array([c]))
@@ -647,7 +660,7 @@ def main():
         value = job_throughput(flops, args.steps, world, elapsed_ms, 1e12)
         # dense peak of the operand type: the measured bf16 burst x the nominal ratio (fp8 4.5 / 2.25 = 2,
         # fp4 13.5 / 2.25 = 6)
-        ratio = 6.0 if args.fmt == "nvfp4" else 2.0
+        ratio = {"nvfp4": 6.0, "fp8": 2.0, "bf16": 1.0}[args.fmt]
         fp8_peak = ratio * pk["bf16_tflops"]
         gflops = 2.0 * int(counts.sum()) * w.N * w.K
         achieved = gflops / (first_gemm_ms / 1e3) / 1e12

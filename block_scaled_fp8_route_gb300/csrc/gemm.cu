@@ -42,6 +42,7 @@ constexpr int kBigTok = 224;        // token tile of the large-segment variant
 constexpr int kHostTok = 448;       // token tile of the host-weight (K-outer / M-inner) variant
 constexpr int kFmtFp8 = 0;          // E4M3 operands, UE8M0 scales per 128 K (kind::mxf8f6f4, 1X)
 constexpr int kFmtNvfp4 = 1;        // E2M1 operands, UE4M3 scales per 16 K (kind::mxf4nvf4, 4X)
+constexpr int kFmtBf16 = 2;         // BF16 operands, no scales (kind::f16)
 constexpr int kNvfp4MaxE = 256;     // NVFP4 variants size their tile tables for 256 experts
 
 struct GemmArgs {
@@ -81,8 +82,9 @@ struct GemmArgs {
 template <int TOK, int CPS = 1, int MAXE = kMaxExperts, int FMT = kFmtFp8>
 struct Cfg {
   static constexpr bool kFp4 = FMT == kFmtNvfp4;
+  static constexpr bool kBf16 = FMT == kFmtBf16;            // no scale factors: SF warps idle
   static constexpr int kMaxE = MAXE;
-  static constexpr int kKElems = kFp4 ? 256 : 128;           // K values per stage
+  static constexpr int kKElems = kFp4 ? 256 : kBf16 ? 64 : 128;   // K values per stage
   static constexpr int kKbPerSlot = kFp4 ? 1 : 4;            // stages per SF slot
   static constexpr int kStages = CPS == 2 ? (TOK <= 64 ? (MAXE <= 256 ? 4 : 3) : TOK <= 128 ? 3 : 2)
                                           : TOK <= 64 ? 8 : TOK <= 224 ? 4 : 2;
@@ -102,7 +104,7 @@ struct Cfg {
   // SF slot: 4 weight-SF columns, then per sub-tile kSub/32 token-SF columns
   // starting every 8 columns (scale-factor TMEM addresses stay 4-column aligned)
   static constexpr int kSubSfCols = kSub / 32;
-  static constexpr int kSfCols = kFp4 ? 32 : TOK <= 64 ? 8 : TOK <= 224 ? 16 : 32;
+  static constexpr int kSfCols = kBf16 ? 0 : kFp4 ? 32 : TOK <= 64 ? 8 : TOK <= 224 ? 16 : 32;
   static __device__ __forceinline__ int tok_sf_col(int c) { return 4 + (c / kSubSfCols) * 8 + c % kSubSfCols; }
   static constexpr int kSfBase = kAccBufs * TOK;
   static constexpr int kTmemUsed = kSfBase + kSfSlots * kSfCols;
@@ -116,7 +118,7 @@ struct Cfg {
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kStageB + kStageA) + kEpiBytes +
                                   kTableBytes + kBarBytes;
   static_assert(kSfBase + kSfSlots * kSfCols <= 512, "TMEM columns");
-  static_assert(4 + (TOK / kSub - 1) * 8 + kSubSfCols <= kSfCols, "SF slot width");
+  static_assert(kBf16 || 4 + (TOK / kSub - 1) * 8 + kSubSfCols <= kSfCols, "SF slot width");
   static_assert(kSubSfCols <= 8, "token SF columns of a sub-tile");
   static_assert(kTmemUsed <= 512, "TMEM budget");
   static_assert(kSmem * CPS + 1024 * CPS <= 233472, "shared memory budget");
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * TOK;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (kb % C::kKbPerSlot == 0) {
+          if (!C::kBf16 && kb % C::kKbPerSlot == 0) {
             if (!mbar_wait(&sf_full[sf_slot], sf_phase, abort_flag, p.err)) { ok = false; break; }
           }
           if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
@@ -333,6 +335,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
           const uint64_t bdesc = smem_desc_k_sw128(smem_u32(stage_a + stage * C::kStageA));
           if constexpr (C::kFp4) {
             // four K = 64 steps; step k's scales: weight words at columns 4k, token words at 16 + 4k
+            // (NVFP4 tiles hold at most 128 tokens: one sub-tile, MMA N = mma_n <= 128)
+            static_assert(!C::kFp4 || TOK == C::kSub, "NVFP4: one MMA sub-tile");
             const uint32_t idesc = idesc_nvf4(kBlockW, mma_n);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -343,18 +347,27 @@ __global__ void __launch_bounds__(kThreads, CPS)
           for (int j = 0; j < TOK / C::kSub; ++j) {
             const int n_j = static_cast<int>(mma_n) - j * C::kSub;
             if (n_j <= 0) break;
-            const uint32_t idesc = idesc_mxf8_e4m3(kBlockW, n_j < C::kSub ? n_j : C::kSub, kb & 3, kb & 3);
+            const uint32_t nn = n_j < C::kSub ? n_j : C::kSub;    // MMA N of this sub-tile: 16..224
             const uint64_t bd = bdesc + static_cast<uint64_t>(j * C::kSub * kBlockK >> 4);
+            if constexpr (C::kBf16) {
+              // four K = 16 steps of 32 bytes inside the swizzled 128-byte rows
+              const uint32_t idesc = idesc_bf16(kBlockW, nn);
 #pragma unroll
-            for (int k = 0; k < kBlockK / 32; ++k) {
-              // advance 32 bytes (one K=32 step of FP8) inside the swizzled 128-byte rows
-              mma_mxf8(d_tmem + j * C::kSub, adesc + 2 * k, bd + 2 * k, idesc, sfw, sft + j * 8, (kb | k) != 0);
+              for (int k = 0; k < 4; ++k)
+                mma_bf16(d_tmem + j * C::kSub, adesc + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+            } else {
+              const uint32_t idesc = idesc_mxf8_e4m3(kBlockW, nn, kb & 3, kb & 3);
+#pragma unroll
+              for (int k = 0; k < kBlockK / 32; ++k) {
+                // advance 32 bytes (one K=32 step of FP8) inside the swizzled 128-byte rows
+                mma_mxf8(d_tmem + j * C::kSub, adesc + 2 * k, bd + 2 * k, idesc, sfw, sft + j * 8, (kb | k) != 0);
+              }
             }
           }
           }
           tc_commit(&empty[stage]);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-          if (kb % C::kKbPerSlot == C::kKbPerSlot - 1 || kb == nkb - 1) {
+          if (!C::kBf16 && (kb % C::kKbPerSlot == C::kKbPerSlot - 1 || kb == nkb - 1)) {
             tc_commit(&sf_empty[sf_slot]);
             if (++sf_slot == C::kSfSlots) { sf_slot = 0; sf_phase ^= 1u; }
           }
@@ -429,7 +442,9 @@ __global__ void __launch_bounds__(kThreads, CPS)
     const int q = warp & 3;
     uint32_t sf_slot = 0, sf_phase = 0;
     bool ok = true;
-    if constexpr (C::kFp4) {
+    if constexpr (C::kBf16) {
+      // no scale factors
+    } else if constexpr (C::kFp4) {
       // NVFP4: per stage, MMA k's word of weight row (lane + 32c) -> column 4k + c, of token
       // row (lane + 32c) -> column 16 + 4k + c; rows past the tile get scale 0
       for (int t = t_first; t < total_tiles && ok; t += G) {
@@ -542,7 +557,7 @@ bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int6
   using C = Cfg<TOK, CPS, MAXE, FMT>;
   if (args.E > MAXE) return BSF_ERR_UNSUPPORTED;
   CUtensorMap map_a, map_b;
-  const int64_t row_bytes = C::kFp4 ? args.K / 2 : args.K;
+  const int64_t row_bytes = C::kFp4 ? args.K / 2 : C::kBf16 ? 2 * args.K : args.K;
   if (!make_map(&map_a, a, args.m_rows, row_bytes, C::kBoxRows)) return BSF_ERR_CUDA;
   if (!make_map(&map_b, b, static_cast<int64_t>(args.E) * args.N, row_bytes, kBlockW)) return BSF_ERR_CUDA;
   static bool attr_set[64] = {false};
@@ -713,4 +728,87 @@ extern "C" bsf_status bsf_grouped_gemm_nvfp4_masked(const uint8_t* a, const int3
   }
   const int64_t max_tiles = E * ((max_m + 127) / 128) * (N / 128);
   return launch<128, 2, kNvfp4MaxE, kFmtNvfp4>(args, a, b, max_tiles, s);
+}
+
+// ---------------------------------------------------------------- BF16
+// Same kernel on unquantised bf16 operands ("AsymGEMM" README, "BF16 Asymmetric
+// GEMM"): kind::f16 MMA with both operands BF16, FP32 accumulation, no scales.
+
+namespace bsf {
+namespace {
+
+bsf_status check_bf16(const void* a, int64_t m_rows, const void* b, const void* d, int64_t E, int64_t N, int64_t K,
+                      int flags, const uint8_t** b_dev) {
+  if (E <= 0 || E > kMaxExperts || N <= 0 || K <= 0 || N % 128 || K % 64) return BSF_ERR_INVALID_ARGUMENT;
+  if (flags & ~(BSF_B_HOST_MAPPED | BSF_DEBUG_WITHHOLD_LOADS)) return BSF_ERR_INVALID_ARGUMENT;
+  if (!a || !b || !d) return BSF_ERR_INVALID_ARGUMENT;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return BSF_ERR_MISALIGNED;
+  if (m_rows > INT32_MAX || E * N > INT32_MAX || K > (1 << 23)) return BSF_ERR_UNSUPPORTED;
+  *b_dev = static_cast<const uint8_t*>(b);
+  if (flags & BSF_B_HOST_MAPPED) {
+    void* db = nullptr;
+    if (cudaHostGetDevicePointer(&db, const_cast<void*>(b), 0) != cudaSuccess) {
+      cudaGetLastError();
+      return BSF_ERR_INVALID_ARGUMENT;
+    }
+    *b_dev = static_cast<const uint8_t*>(db);
+  }
+  return BSF_OK;
+}
+
+}  // namespace
+}  // namespace bsf
+
+extern "C" bsf_status bsf_grouped_gemm_bf16_contig(const void* a, int64_t m_cap, const void* b, void* d,
+                                                   const int32_t* seg_start, const int32_t* counts, int64_t E,
+                                                   int64_t N, int64_t K, int flags, bsf_stream_t stream) {
+  if (m_cap <= 0) return m_cap == 0 ? BSF_OK : BSF_ERR_INVALID_ARGUMENT;
+  const uint8_t* bd = nullptr;
+  bsf_status st = check_bf16(a, m_cap, b, d, E, N, K, flags, &bd);
+  if (st != BSF_OK) return st;
+  if (!seg_start || !counts) return BSF_ERR_INVALID_ARGUMENT;
+  int* err = device_error_ptr();
+  if (!err) return BSF_ERR_CUDA;
+  GemmArgs args{seg_start, counts, 0, m_cap, nullptr, 0, nullptr, static_cast<uint16_t*>(d),
+                static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
+                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint8_t* ad = static_cast<const uint8_t*>(a);
+  if (flags & BSF_B_HOST_MAPPED) {
+    const int64_t max_tiles = (m_cap / kHostTok + E) * (N / 128);
+    return launch<kHostTok, 1, kMaxExperts, kFmtBf16>(args, ad, bd, max_tiles, s);
+  }
+  const int64_t max_tiles = (m_cap / kBigTok + E) * (N / 128);
+  return launch<kBigTok, 2, kMaxExperts, kFmtBf16>(args, ad, bd, max_tiles, s);
+}
+
+extern "C" bsf_status bsf_grouped_gemm_bf16_masked(const void* a, const void* b, void* d, const int32_t* masked_m,
+                                                   int64_t E, int64_t max_m, int64_t N, int64_t K,
+                                                   int64_t expected_m, int flags, bsf_stream_t stream) {
+  if (max_m <= 0) return BSF_ERR_INVALID_ARGUMENT;
+  const int64_t m_rows = E * max_m;
+  const uint8_t* bd = nullptr;
+  bsf_status st = check_bf16(a, m_rows, b, d, E, N, K, flags, &bd);
+  if (st != BSF_OK) return st;
+  if (!masked_m) return BSF_ERR_INVALID_ARGUMENT;
+  int* err = device_error_ptr();
+  if (!err) return BSF_ERR_CUDA;
+  GemmArgs args{nullptr, masked_m, max_m, m_rows, nullptr, 0, nullptr, static_cast<uint16_t*>(d),
+                static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
+                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint8_t* ad = static_cast<const uint8_t*>(a);
+  const int64_t hint = expected_m > 0 ? expected_m : max_m;
+  const bool host = (flags & BSF_B_HOST_MAPPED) != 0;
+  if (max_m <= 64 || (!host && hint <= 32)) {
+    const int64_t max_tiles = E * ((max_m + 63) / 64) * (N / 128);
+    if (E <= 256) return launch<64, 2, 256, kFmtBf16>(args, ad, bd, max_tiles, s);
+    return launch<64, 2, kMaxExperts, kFmtBf16>(args, ad, bd, max_tiles, s);
+  }
+  if (host && max_m > kBigTok) {
+    const int64_t max_tiles = E * ((max_m + kHostTok - 1) / kHostTok) * (N / 128);
+    return launch<kHostTok, 1, kMaxExperts, kFmtBf16>(args, ad, bd, max_tiles, s);
+  }
+  const int64_t max_tiles = E * ((max_m + kBigTok - 1) / kBigTok) * (N / 128);
+  return launch<kBigTok, 2, kMaxExperts, kFmtBf16>(args, ad, bd, max_tiles, s);
 }

@@ -283,11 +283,14 @@ extern "C" size_t bsf_route_workspace_bytes(int64_t T, int64_t kr, int64_t E) {
 namespace bsf {
 namespace {
 
-// bsf_route / bsf_route_nvfp4: nvfp4 selects the scatter's row format.
+enum RowFormat { kRowsFp8, kRowsNvfp4, kRowsBf16 };
+
+// bsf_route / bsf_route_nvfp4 / bsf_route_bf16: fmt selects the scatter's row format
+// (FP8: K bytes + ceil(K/512) SF words; NVFP4: K/2 bytes + K/64 words; BF16: 2K bytes, no SF).
 bsf_status route_impl(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout, int64_t align_or_max_m,
                       int32_t* counts, int32_t* seg_start, int32_t* output_index, int32_t* token_of_row,
                       int32_t* m_indices, int64_t m_cap, const uint8_t* q, const int32_t* sf, int64_t sf_ld,
-                      int64_t K, bool nvfp4, uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld,
+                      int64_t K, RowFormat fmt, uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld,
                       void* workspace, size_t workspace_bytes, bsf_stream_t stream) {
   if (T < 0 || kr <= 0 || E <= 0 || E > kMaxExperts) return BSF_ERR_INVALID_ARGUMENT;
   if (layout != BSF_LAYOUT_CONTIGUOUS && layout != BSF_LAYOUT_MASKED) return BSF_ERR_INVALID_ARGUMENT;
@@ -298,8 +301,12 @@ bsf_status route_impl(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E,
   if (m_cap < need_cap || m_cap > INT32_MAX) return BSF_ERR_INVALID_ARGUMENT;
   if (R > INT32_MAX) return BSF_ERR_UNSUPPORTED;
   if (workspace_bytes < bsf_route_workspace_bytes(T, kr, E) || !workspace) return BSF_ERR_INVALID_ARGUMENT;
-  if (q) {
-    if (!sf || !a_packed || !sfa_packed || K <= 0 || K % (nvfp4 ? 64 : 128)) return BSF_ERR_INVALID_ARGUMENT;
+  if (q && fmt == kRowsBf16) {
+    if (!a_packed || K <= 0 || K % 8) return BSF_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(a_packed)) return BSF_ERR_MISALIGNED;
+  } else if (q) {
+    if (!sf || !a_packed || !sfa_packed || K <= 0 || K % (fmt == kRowsNvfp4 ? 64 : 128))
+      return BSF_ERR_INVALID_ARGUMENT;
     if (sf_ld < T || sf_ld % 4 || sfa_ld < m_cap || sfa_ld % 4) return BSF_ERR_INVALID_ARGUMENT;
     if (!aligned16(q) || !aligned16(a_packed) || !aligned16(sf) || !aligned16(sfa_packed)) return BSF_ERR_MISALIGNED;
   }
@@ -327,8 +334,9 @@ bsf_status route_impl(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E,
   const int64_t fill_blocks = (m_cap + kFillRows - 1) / kFillRows;
   if (fill_blocks > 0) {
     route_fill_kernel<<<static_cast<unsigned>(fill_blocks), kThreads, 0, s>>>(
-        e32, m_cap, counts, seg_start, token_of_row, m_indices, q, sf, sf_ld, nvfp4 ? K / 2 : K,
-        nvfp4 ? K / 64 : (K + 511) / 512, a_packed, sfa_packed, sfa_ld);
+        e32, m_cap, counts, seg_start, token_of_row, m_indices, q, sf, sf_ld,
+        fmt == kRowsNvfp4 ? K / 2 : fmt == kRowsBf16 ? 2 * K : K,
+        fmt == kRowsNvfp4 ? K / 64 : fmt == kRowsBf16 ? 0 : (K + 511) / 512, a_packed, sfa_packed, sfa_ld);
   }
   return launch_status();
 }
@@ -342,7 +350,7 @@ extern "C" bsf_status bsf_route(const int32_t* topk_ids, int64_t T, int64_t kr, 
                                 const int32_t* sf, int64_t sf_ld, int64_t K, uint8_t* a_packed, int32_t* sfa_packed,
                                 int64_t sfa_ld, void* workspace, size_t workspace_bytes, bsf_stream_t stream) {
   return route_impl(topk_ids, T, kr, E, layout, align_or_max_m, counts, seg_start, output_index, token_of_row,
-                    m_indices, m_cap, q, sf, sf_ld, K, false, a_packed, sfa_packed, sfa_ld, workspace,
+                    m_indices, m_cap, q, sf, sf_ld, K, kRowsFp8, a_packed, sfa_packed, sfa_ld, workspace,
                     workspace_bytes, stream);
 }
 
@@ -353,8 +361,18 @@ extern "C" bsf_status bsf_route_nvfp4(const int32_t* topk_ids, int64_t T, int64_
                                       uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld, void* workspace,
                                       size_t workspace_bytes, bsf_stream_t stream) {
   return route_impl(topk_ids, T, kr, E, layout, align_or_max_m, counts, seg_start, output_index, token_of_row,
-                    m_indices, m_cap, q, sf, sf_ld, K, true, a_packed, sfa_packed, sfa_ld, workspace,
+                    m_indices, m_cap, q, sf, sf_ld, K, kRowsNvfp4, a_packed, sfa_packed, sfa_ld, workspace,
                     workspace_bytes, stream);
+}
+
+extern "C" bsf_status bsf_route_bf16(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout,
+                                     int64_t align_or_max_m, int32_t* counts, int32_t* seg_start,
+                                     int32_t* output_index, int32_t* token_of_row, int32_t* m_indices, int64_t m_cap,
+                                     const void* x, int64_t K, void* a_packed, void* workspace,
+                                     size_t workspace_bytes, bsf_stream_t stream) {
+  return route_impl(topk_ids, T, kr, E, layout, align_or_max_m, counts, seg_start, output_index, token_of_row,
+                    m_indices, m_cap, static_cast<const uint8_t*>(x), nullptr, 0, K, kRowsBf16,
+                    static_cast<uint8_t*>(a_packed), nullptr, 0, workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -105,7 +105,10 @@ class RouteBuffers:
         ws = _lib.load().bsf_route_workspace_bytes(T, kr, E)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
         self.fmt = fmt
-        if scatter and K and fmt == "nvfp4":
+        if scatter and K and fmt == "bf16":
+            self.a_packed = torch.empty((max(self.m_cap, 1), K), dtype=torch.bfloat16, device=device)
+            self.sfa_packed = None
+        elif scatter and K and fmt == "nvfp4":
             self.a_packed = torch.empty((max(self.m_cap, 1), K // 2), dtype=torch.uint8, device=device)
             self.sfa_packed = torch.empty((K // 64, sf_ld(self.m_cap)), dtype=torch.int32, device=device)
         elif scatter and K:
@@ -116,13 +119,22 @@ class RouteBuffers:
 
 
 def route(topk_ids, E, layout, align_or_max_m, q=None, sf=None, bufs=None, stream=None, fmt="fp8"):
-    """Routing + optional scatter of quantised rows (``fmt`` "fp8" or "nvfp4"); returns a RouteBuffers."""
+    """Routing + optional scatter of quantised rows (``fmt`` "fp8" or "nvfp4") or of bf16 rows
+    (``fmt`` "bf16", ``q`` the bf16 activations, no ``sf``); returns a RouteBuffers."""
     T, kr = topk_ids.shape
     K = (q.shape[1] * (2 if fmt == "nvfp4" else 1)) if q is not None else 0
     if bufs is None:
         bufs = RouteBuffers(T, kr, E, layout, align_or_max_m, K=K, device=topk_ids.device, scatter=q is not None,
                             fmt=fmt)
     lib = _lib.load()
+    if fmt == "bf16":
+        _lib.check(lib.bsf_route_bf16(
+            _ptr(topk_ids.contiguous()), T, kr, E, layout, align_or_max_m,
+            _ptr(bufs.counts), _ptr(bufs.seg_start), _ptr(bufs.output_index), _ptr(bufs.token_of_row),
+            _ptr(bufs.m_indices), bufs.m_cap, _ptr(q.contiguous() if q is not None else None), K,
+            _ptr(bufs.a_packed) if q is not None else None, _ptr(bufs.workspace), bufs.workspace.numel(),
+            _stream(stream)), "route_bf16")
+        return bufs
     fn = lib.bsf_route_nvfp4 if fmt == "nvfp4" else lib.bsf_route
     _lib.check(fn(
         _ptr(topk_ids.contiguous()), T, kr, E, layout, align_or_max_m,
@@ -276,4 +288,29 @@ def grouped_gemm_nvfp4_masked(a, sfa, a_exp, b, sfb, b_exp, masked_m, max_m, d=N
     _lib.check(_lib.load().bsf_grouped_gemm_nvfp4_masked(
         _ptr(a), _ptr(sfa), sfa.shape[1], int(a_exp), _ptr(b), _ptr(sfb), _ptr(b_exp), _ptr(d), _ptr(masked_m),
         E, max_m, N, 2 * K2, expected_m, flags, _stream(stream)), "grouped_gemm_nvfp4_masked")
+    return d
+
+
+# ----------------------------------------------------------------------------- BF16
+def grouped_gemm_bf16_contig(a, b, seg_start, counts, d=None, flags=0, stream=None):
+    """a bf16 [m_cap, K], b bf16 [E, N, K] -> d bf16 [m_cap, N] (segment rows written)."""
+    m_cap, K = a.shape
+    E, N, _ = b.shape
+    if d is None:
+        d = torch.empty((m_cap, N), dtype=torch.bfloat16, device=a.device)
+    _lib.check(_lib.load().bsf_grouped_gemm_bf16_contig(
+        _ptr(a), m_cap, _ptr(b), _ptr(d), _ptr(seg_start), _ptr(counts), E, N, K, flags, _stream(stream)),
+        "grouped_gemm_bf16_contig")
+    return d
+
+
+def grouped_gemm_bf16_masked(a, b, masked_m, max_m, d=None, expected_m=0, flags=0, stream=None):
+    """a bf16 [E*max_m, K], b bf16 [E, N, K] -> d bf16 [E*max_m, N]."""
+    K = a.shape[-1]
+    E, N, _ = b.shape
+    if d is None:
+        d = torch.empty((E * max_m, N), dtype=torch.bfloat16, device=a.device)
+    _lib.check(_lib.load().bsf_grouped_gemm_bf16_masked(
+        _ptr(a), _ptr(b), _ptr(d), _ptr(masked_m), E, max_m, N, K, expected_m, flags, _stream(stream)),
+        "grouped_gemm_bf16_masked")
     return d

@@ -18,8 +18,9 @@ from . import ops
 
 
 class MoEPath:
-    """``fmt`` = "fp8" (E4M3, UE8M0 per 1 x 128 / 128 x 128) or "nvfp4" (E2M1, UE4M3 per 1 x 16, a
-    power-of-two tensor exponent per expert for the weights and ``a_exp`` for the activations)."""
+    """``fmt`` = "fp8" (E4M3, UE8M0 per 1 x 128 / 128 x 128), "nvfp4" (E2M1, UE4M3 per 1 x 16, a
+    power-of-two tensor exponent per expert for the weights and ``a_exp`` for the activations) or
+    "bf16" (unquantised operands; the route scatters bf16 rows)."""
 
     def __init__(self, E, kr, T, K, N, w_bf16, layout=ops.CONTIGUOUS, align_or_max_m=1, w2_bf16=None,
                  device="cuda", weights_on_host=False, expected_m=0, fused_dispatch=None, fmt="fp8", a_exp=0):
@@ -38,6 +39,8 @@ class MoEPath:
             self.w2q, self.sfb2, self.b2_exp = self._weights(w2_bf16.to(device), self.K2)
         self.bufs = ops.RouteBuffers(T, kr, E, layout, align_or_max_m, K=K, device=device, fmt=fmt)
         self.fused_dispatch = ops.dispatch_supported(T, kr, E) if fused_dispatch is None else fused_dispatch
+        if fmt == "bf16":
+            self.fused_dispatch = False          # nothing to quantise: the route scatters the bf16 rows
         m = self.bufs.m_cap
         self.q, self.sf = self._act_buffers(T, K, device)
         self.y = torch.empty((max(m, 1), N), dtype=torch.bfloat16, device=device)
@@ -49,12 +52,16 @@ class MoEPath:
             self.z = torch.empty((T, N), dtype=torch.bfloat16, device=device)
 
     def _weights(self, w, K):
+        if self.fmt == "bf16":
+            return w.contiguous(), None, None
         if self.fmt == "nvfp4":
             return ops.quantise_weight_nvfp4(w)
         wq, sf128 = ops.quantise_weight(w)
         return wq, ops.prepare_weight_sf(sf128, K), None
 
     def _act_buffers(self, rows, K, device):
+        if self.fmt == "bf16":
+            return None, None
         if self.fmt == "nvfp4":
             return (torch.empty((rows, K // 2), dtype=torch.uint8, device=device),
                     torch.empty((K // 64, ops.sf_ld(rows)), dtype=torch.int32, device=device))
@@ -72,14 +79,20 @@ class MoEPath:
             n = 1                                                  # dispatch
         else:
             small = ops.dispatch_supported(self.T, self.kr, self.E)
-            n = 1 + (2 if small else 4)                            # quantise + route (+ fill)
+            quant = 0 if self.fmt == "bf16" else 1
+            n = quant + (2 if small else 4)                        # quantise + route (+ fill)
         n += 1                                                     # grouped GEMM
         if self.two_gemms:
-            n += 2                                                 # quantise of h2 + second GEMM
+            n += 1 if self.fmt == "bf16" else 2                    # (quantise of h2 +) second GEMM
         return n + 1                                               # combine
 
     def gemm(self, a, sfa, wq, sfb, d, b_exp=None):
         b = self.bufs
+        if self.fmt == "bf16":
+            if self.layout == ops.MASKED:
+                return ops.grouped_gemm_bf16_masked(a, wq, b.counts, self.align_or_max_m, d=d,
+                                                    expected_m=self.expected_m, flags=self.flags)
+            return ops.grouped_gemm_bf16_contig(a, wq, b.seg_start, b.counts, d=d, flags=self.flags)
         if self.fmt == "nvfp4":
             if self.layout == ops.MASKED:
                 return ops.grouped_gemm_nvfp4_masked(a, sfa, self.a_exp, wq, sfb, b_exp, b.counts,
@@ -101,13 +114,17 @@ class MoEPath:
                                bufs=self.bufs)
         elif self.fused_dispatch:
             ops.dispatch(x, topk_ids, self.E, self.layout, self.align_or_max_m, bufs=self.bufs)
+        elif self.fmt == "bf16":
+            ops.route(topk_ids, self.E, self.layout, self.align_or_max_m, q=x, bufs=self.bufs, fmt="bf16")
         else:
             self._quantise(x, self.q, self.sf)
             ops.route(topk_ids, self.E, self.layout, self.align_or_max_m, q=self.q, sf=self.sf, bufs=self.bufs,
                       fmt=self.fmt)
         self.gemm(self.bufs.a_packed, self.bufs.sfa_packed, self.wq, self.sfb, self.y, self.b_exp)
         out = self.y
-        if self.two_gemms:
+        if self.two_gemms and self.fmt == "bf16":
+            self.gemm(h2, None, self.w2q, None, self.y2)
+        elif self.two_gemms:
             self._quantise(h2, self.q2, self.sf2)
             self.gemm(self.q2, self.sf2, self.w2q, self.sfb2, self.y2, self.b2_exp)
             out = self.y2

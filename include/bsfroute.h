@@ -358,6 +358,35 @@ bsf_status bsf_grouped_gemm_nvfp4_masked(const uint8_t* a, const int32_t* sfa, i
                                          const int32_t* masked_m, int64_t E, int64_t max_m, int64_t N, int64_t K,
                                          int64_t expected_m, int flags, bsf_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * BF16 operands ("AsymGEMM" README, "BF16 Asymmetric GEMM": a bf16 [M, K],
+ * b bf16 [G, N, K], d bf16 [M, N]; contiguous and masked layouts as for FP8).
+ */
+
+/* bsf_route_bf16 — bsf_route whose scatter copies bf16 rows: x bf16 [T, K]
+ * (K % 8 == 0) into a_packed bf16 [m_cap, K] (routed rows written, padding
+ * rows left as they were).  Routing outputs, workspace and errors as in
+ * bsf_route; x may be NULL (indices only). */
+bsf_status bsf_route_bf16(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout,
+                          int64_t align_or_max_m, int32_t* counts, int32_t* seg_start, int32_t* output_index,
+                          int32_t* token_of_row, int32_t* m_indices, int64_t m_cap, const void* x, int64_t K,
+                          void* a_packed, void* workspace, size_t workspace_bytes, bsf_stream_t stream);
+
+/* bsf_grouped_gemm_bf16_contig / _masked — D[r, n] = BF16( sum_k A[r, k] B_e[n, k] )
+ * for the rows of each expert (contiguous segments seg_start / counts, or
+ * masked slots of max_m rows with masked_m valid): FP32 accumulation on the
+ * tensor cores (kind::f16, both operands BF16), round-to-nearest-even to
+ * bf16.  a bf16 [rows, K], b bf16 [E, N, K] (device, or pinned host with
+ * BSF_B_HOST_MAPPED), d bf16 [rows, N] (only the rows above are written).
+ * Needs K % 64 == 0, N % 128 == 0, 16-byte aligned a, b, d.  Ownership,
+ * launch order and errors as in the FP8 calls. */
+bsf_status bsf_grouped_gemm_bf16_contig(const void* a, int64_t m_cap, const void* b, void* d,
+                                        const int32_t* seg_start, const int32_t* counts, int64_t E, int64_t N,
+                                        int64_t K, int flags, bsf_stream_t stream);
+bsf_status bsf_grouped_gemm_bf16_masked(const void* a, const void* b, void* d, const int32_t* masked_m, int64_t E,
+                                        int64_t max_m, int64_t N, int64_t K, int64_t expected_m, int flags,
+                                        bsf_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
