@@ -18,7 +18,8 @@ Sources (page title, section):
   (calc_diff tolerance, repeat-run determinism).
 * "AsymGEMM" README, "Token Layout Protocols" (contiguous and masked layouts),
   "FP4 Asymmetric GEMM" (NVFP4 operands, ``oracle/nvfp4.py``), "BF16 Asymmetric
-  GEMM" (``oracle/bf16.py``).
+  GEMM" (``oracle/bf16.py``), notation ``disable_ue8m0_cast`` (float32 scale
+  factors, ``oracle/f32sf.py``).
 * "CuTeDSL bei Perplexity", Blackwell support (16-element absolute maximum
   of the NVFP4 quantiser).
 
@@ -28,4 +29,4 @@ values the pages print, closed forms, library routines or brute force, except
 the GPU-internal FP32 accumulation order, which is outside the oracle.
 """
 
-from . import formats, quantise, route, gemm, combine, checks, nvfp4, bf16  # noqa: F401
+from . import formats, quantise, route, gemm, combine, checks, nvfp4, bf16, f32sf  # noqa: F401

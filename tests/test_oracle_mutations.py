@@ -145,3 +145,21 @@ def test_bf16_wrong_expert_weights_are_caught(monkeypatch):
     monkeypatch.setattr(bf16_oracle, "grouped_gemm",
                         lambda a, b, seg, counts: orig(a, np.roll(b, 1, axis=0), seg, counts))
     _fails(pin_bf16.test_exact_rational_brute_force)
+
+
+# ---------------------------------------------------------------- FP32 scale factors
+from oracle import f32sf  # noqa: E402
+from tests import test_oracle_f32sf as pin_f32sf  # noqa: E402
+
+
+def test_f32sf_wrong_divisor_is_caught(monkeypatch):
+    monkeypatch.setattr(f32sf, "_scale", lambda amax32: np.where(amax32 == 0, np.float32(1.0),
+                                                                 amax32 / np.float32(224.0)).astype(np.float32))
+    _fails(pin_f32sf.test_hand_computed_blocks)
+
+
+def test_f32sf_dropped_weight_scale_is_caught(monkeypatch):
+    orig = f32sf.grouped_gemm
+    monkeypatch.setattr(f32sf, "grouped_gemm",
+                        lambda aq, as_, bq, bs, seg, counts: orig(aq, as_, bq, np.ones_like(bs), seg, counts))
+    _fails(pin_f32sf.test_gemm_exact_rational_brute_force)
