@@ -43,8 +43,9 @@ def parse():
                     help="token counts of the host-weight sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--fmt", default="fp8", choices=["fp8", "nvfp4", "bf16"],
-                    help="operand format: FP8 E4M3 with UE8M0 scales, NVFP4 (E2M1, UE4M3 per 16) or BF16")
+    ap.add_argument("--fmt", default="fp8", choices=["fp8", "nvfp4", "bf16", "fp8_f32sf"],
+                    help="operand format: FP8 E4M3 with UE8M0 scales, NVFP4 (E2M1, UE4M3 per 16), BF16, "
+                         "or FP8 with float32 scales")
     ap.add_argument("--no-fused-dispatch", action="store_true",
                     help="quantise + route as separate launches even where the single-launch dispatch applies")
     ap.add_argument("--no-large-m", action="store_true",
@@ -81,7 +82,8 @@ def job_throughput(units_per_step, steps, world, elapsed_ms, scale):
 # ----------------------------------------------------------------------------- work accounting
 DTYPES = {"fp8": "e4m3 x e4m3 -> f32 acc -> bf16",
           "nvfp4": "e2m1 x e2m1 (ue4m3 per 16, 2^j per tensor) -> f32 acc -> bf16",
-          "bf16": "bf16 x bf16 -> f32 acc -> bf16"}
+          "bf16": "bf16 x bf16 -> f32 acc -> bf16",
+          "fp8_f32sf": "e4m3 x e4m3 (f32 scales per 128-K block, applied on CUDA cores) -> f32 acc -> bf16"}
 
 
 def operand_bytes(K, fmt):
@@ -91,7 +93,18 @@ def operand_bytes(K, fmt):
         return K // 2, K // 16
     if fmt == "bf16":
         return 2 * K, 0
+    if fmt == "fp8_f32sf":
+        return K, (K // 128) * 4
     return K, ((K // 128 + 3) // 4) * 4
+
+
+def weight_bytes(N, K, fmt):
+    """Bytes of one expert's weights and the weight scales the GEMM reads: per-row packed UE8M0
+    words (FP8), per-row UE4M3 bytes (NVFP4), one float32 per 128 x 128 block (FP32 scales)."""
+    if fmt == "fp8_f32sf":
+        return N * K + (N // 128) * (K // 128) * 4
+    qb, sb = operand_bytes(K, fmt)
+    return N * (qb + sb)
 
 
 def step_work(w, counts, placed_rows, fused_dispatch=False, fmt="fp8"):
@@ -111,7 +124,7 @@ def step_work(w, counts, placed_rows, fused_dispatch=False, fmt="fp8"):
     else:
         b["quantise"] = T * K * 2 + T * (qb + sb)
         b["route"] = R * 4 + R * 4 + placed_rows * 8 + rows * 2 * (qb + sb)
-    gemm_bytes = len(active) * N * (qb + sb) + rows * (qb + sb + N * 2)
+    gemm_bytes = len(active) * weight_bytes(N, K, fmt) + rows * (qb + sb + N * 2)
     flops = 2.0 * rows * N * K
     b["gemm"] = gemm_bytes
     out_n = N
@@ -119,7 +132,7 @@ def step_work(w, counts, placed_rows, fused_dispatch=False, fmt="fp8"):
         qb2, sb2 = operand_bytes(w.K2, fmt)
         if fmt != "bf16":
             b["quantise2"] = placed_rows * w.K2 * 2 + placed_rows * (qb2 + sb2)
-        b["gemm2"] = len(active) * w.N2 * (qb2 + sb2) + rows * (qb2 + sb2 + w.N2 * 2)
+        b["gemm2"] = len(active) * weight_bytes(w.N2, w.K2, fmt) + rows * (qb2 + sb2 + w.N2 * 2)
         flops += 2.0 * rows * w.N2 * w.K2
         out_n = w.N2
     b["combine"] = R * out_n * 2 + T * out_n * 2 + R * 8
@@ -286,6 +299,8 @@ class OracleSample:
         wb = wt.view(torch.int16).numpy().view(np.uint16)
         if fmt == "bf16":
             self.bq, self.bsf = wb, None
+        elif fmt == "fp8_f32sf":
+            self.bq, self.bsf = oracle.f32sf.quantise_weight(wb)
         elif fmt == "nvfp4":
             wv = oracle.formats.bf16_bits_to_f64(wb)
             self.bj = oracle.nvfp4.global_exponent(np.abs(wv).reshape(len(self.experts), -1).max(axis=1))
@@ -297,9 +312,11 @@ class OracleSample:
 
     def run(self):
         o, w = self.oracle, self.w
-        fp4, bf = self.fmt == "nvfp4", self.fmt == "bf16"
+        fp4, bf, f32 = self.fmt == "nvfp4", self.fmt == "bf16", self.fmt == "fp8_f32sf"
         t0 = time.perf_counter()
-        if bf:
+        if f32:
+            aq, asf = o.f32sf.quantise_act(self.xb)
+        elif bf:
             aq, asf = self.xb, np.zeros((self.xb.shape[0], 1), dtype=np.uint8)
         elif fp4:
             aq, _, asf = o.nvfp4.quantise_act(self.xb, 0)
@@ -307,12 +324,15 @@ class OracleSample:
             aq, asf = o.quantise.quantise_act(self.xb)
         r = o.route.route(self.ids, w.E, w.layout, align=w.align, max_m=w.max_m)
         a_rows = o.route.scatter_rows(aq, r["token_of_row"])
-        a_sf = o.route.scatter_rows(asf, r["token_of_row"], pad_value=0 if fp4 else 127)
+        a_sf = o.route.scatter_rows(asf, r["token_of_row"], pad_value=1.0 if f32 else 0 if fp4 else 127)
         y = np.zeros((r["rows_used"], w.N), dtype=np.uint16)
         rows = 0
         for i, e in enumerate(self.experts):
             s, c = int(r["seg_start"][e]), int(r["counts"][e])
-            if bf:
+            if f32:
+                y[s:s + c], _ = o.f32sf.grouped_gemm(a_rows[s:s + c], a_sf[s:s + c], self.bq[i:i + 1],
+                                                     self.bsf[i:i + 1], np.array([0, c]), np.array([c]))
+            elif bf:
                 y[s:s + c], _ = o.bf16.grouped_gemm(a_rows[s:s + c], self.bq[i:i + 1], np.array([0, c]),
                                                     np.array([c]))
             elif fp4:
@@ -325,7 +345,7 @@ class OracleSample:
         o.combine.combine(y, r["output_index"], self.p)
         dt = time.perf_counter() - t0
         qb, sb = operand_bytes(w.K, self.fmt)
-        byts = len(self.experts) * w.N * (qb + sb) + rows * (qb + sb + w.N * 2)
+        byts = len(self.experts) * weight_bytes(w.N, w.K, self.fmt) + rows * (qb + sb + w.N * 2)
         return dt, byts, 2.0 * rows * w.N * w.K
 
 
@@ -344,8 +364,7 @@ def workload_config(w, fmt="fp8"):
         cfg.update({"K2": w.K2, "N2": w.N2})
     if fmt != "fp8":
         cfg["format"] = fmt
-        qb, sb = operand_bytes(w.K, fmt)
-        cfg["l2"] = f"no flush: weights {(w.E * w.N * (qb + sb)) / 1e9:.2f} GB > 129 MB L2, streamed each step"
+        cfg["l2"] = f"no flush: weights {(w.E * weight_bytes(w.N, w.K, fmt)) / 1e9:.2f} GB > 129 MB L2, streamed each step"
     return cfg
 
 
@@ -660,7 +679,7 @@ def main():
         value = job_throughput(flops, args.steps, world, elapsed_ms, 1e12)
         # dense peak of the operand type: the measured bf16 burst x the nominal ratio (fp8 4.5 / 2.25 = 2,
         # fp4 13.5 / 2.25 = 6)
-        ratio = {"nvfp4": 6.0, "fp8": 2.0, "bf16": 1.0}[args.fmt]
+        ratio = {"nvfp4": 6.0, "fp8": 2.0, "fp8_f32sf": 2.0, "bf16": 1.0}[args.fmt]
         fp8_peak = ratio * pk["bf16_tflops"]
         gflops = 2.0 * int(counts.sum()) * w.N * w.K
         achieved = gflops / (first_gemm_ms / 1e3) / 1e12

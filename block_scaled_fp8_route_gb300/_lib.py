@@ -40,6 +40,13 @@ SIGNATURES = {
                                 _size, _p]),
     "bsf_grouped_gemm_bf16_contig": (_c_int, [_p, _i64, _p, _p, _p, _p, _i64, _i64, _i64, _c_int, _p]),
     "bsf_grouped_gemm_bf16_masked": (_c_int, [_p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _c_int, _p]),
+    "bsf_quantise_act_f32sf": (_c_int, [_p, _i64, _i64, _p, _p, _i64, _p]),
+    "bsf_quantise_weight_f32sf": (_c_int, [_p, _i64, _i64, _i64, _p, _p, _p]),
+    "bsf_route_f32sf": (_c_int, [_p, _i64, _i64, _i64, _c_int, _i64, _p, _p, _p, _p, _p, _i64,
+                                 _p, _p, _i64, _i64, _p, _p, _i64, _p, _size, _p]),
+    "bsf_grouped_gemm_f32sf_contig": (_c_int, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p, _i64, _i64, _i64, _c_int,
+                                               _p]),
+    "bsf_grouped_gemm_f32sf_masked": (_c_int, [_p, _p, _i64, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _c_int, _p]),
     "bsf_nvfp4_tensor_exponent": (_c_int, [_p, _i64, _i64, _p, _p]),
     "bsf_quantise_act_nvfp4": (_c_int, [_p, _i64, _i64, _c_int, _p, _p, _i64, _p]),
     "bsf_quantise_weight_nvfp4": (_c_int, [_p, _i64, _i64, _i64, _p, _p, _p, _p]),

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(BUILD_DIR, "libbsfroute.so")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH_FLAGS + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-I" + os.path.join(ROOT, "include")]
-SOURCES = ["api.cu", "quantise.cu", "nvfp4.cu", "route.cu", "dispatch.cu", "gemm.cu", "combine.cu"]
+SOURCES = ["api.cu", "quantise.cu", "nvfp4.cu", "f32sf.cu", "route.cu", "dispatch.cu", "gemm.cu", "combine.cu"]
 
 
 def _nvcc():

@@ -179,6 +179,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// E4M3 x E4M3 -> FP32 without scale factors (kind::f8f6f4, K = 32 per instruction).
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
                "r"(v2), "r"(v3)
@@ -254,6 +265,16 @@ __device__ __forceinline__ uint32_t idesc_bf16(uint32_t m, uint32_t n) {
   d |= 1u << 4;               // D format F32
   d |= 1u << 7;               // A format BF16
   d |= 1u << 10;              // B format BF16
+  d |= (n >> 3) << 17;        // N / 8
+  d |= (m >> 4) << 24;        // M / 16
+  return d;
+}
+
+// Instruction descriptor for kind::f8f6f4 without block scaling: A and B E4M3
+// (format 0), FP32 accumulator (bits 4-5 = 1), K-major.
+__device__ __forceinline__ uint32_t idesc_f8(uint32_t m, uint32_t n) {
+  uint32_t d = 0;
+  d |= 1u << 4;               // D format F32
   d |= (n >> 3) << 17;        // N / 8
   d |= (m >> 4) << 24;        // M / 16
   return d;

@@ -43,6 +43,7 @@ constexpr int kHostTok = 448;       // token tile of the host-weight (K-outer / 
 constexpr int kFmtFp8 = 0;          // E4M3 operands, UE8M0 scales per 128 K (kind::mxf8f6f4, 1X)
 constexpr int kFmtNvfp4 = 1;        // E2M1 operands, UE4M3 scales per 16 K (kind::mxf4nvf4, 4X)
 constexpr int kFmtBf16 = 2;         // BF16 operands, no scales (kind::f16)
+constexpr int kFmtFp8F32 = 3;       // E4M3 operands, float32 scales applied in software per 128-K block
 constexpr int kNvfp4MaxE = 256;     // NVFP4 variants size their tile tables for 256 experts
 
 struct GemmArgs {
@@ -59,6 +60,8 @@ struct GemmArgs {
   int withhold_loads;        // test-only fault injection (BSF_DEBUG_WITHHOLD_LOADS)
   int a_exp;                 // NVFP4: tensor exponent of A
   const int32_t* b_exp;      // NVFP4: tensor exponent per expert of B [E]
+  const float* sfa_f32;      // FP32 scales: A [K/128][sfa_ld]
+  const float* sfb_f32;      // FP32 scales: B [E][N/128][K/128]
 };
 
 // TOK = token columns of one tile's accumulator.  64 and 224 keep two
@@ -83,12 +86,15 @@ template <int TOK, int CPS = 1, int MAXE = kMaxExperts, int FMT = kFmtFp8>
 struct Cfg {
   static constexpr bool kFp4 = FMT == kFmtNvfp4;
   static constexpr bool kBf16 = FMT == kFmtBf16;            // no scale factors: SF warps idle
+  // float32 scales: each 128-K stage is multiplied into its own TMEM partial (two buffers),
+  // which the epilogue warps scale and add into registers (the SF warps idle)
+  static constexpr bool kF32 = FMT == kFmtFp8F32;
   static constexpr int kMaxE = MAXE;
   static constexpr int kKElems = kFp4 ? 256 : kBf16 ? 64 : 128;   // K values per stage
   static constexpr int kKbPerSlot = kFp4 ? 1 : 4;            // stages per SF slot
   static constexpr int kStages = CPS == 2 ? (TOK <= 64 ? (MAXE <= 256 ? 4 : 3) : TOK <= 128 ? 3 : 2)
                                           : TOK <= 64 ? 8 : TOK <= 224 ? 4 : 2;
-  static constexpr int kAccBufs = (CPS == 1 && TOK <= 224) ? 2 : 1;
+  static constexpr int kAccBufs = (kF32 || (CPS == 1 && TOK <= 224)) ? 2 : 1;
   static constexpr int kSfSlots = kFp4 ? 4 : (CPS == 1 && TOK <= 224) ? 4 : 2;
   static constexpr int kTokSfCols = (TOK + 31) / 32;
   static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK <= 128 ? 64 : TOK <= 224 ? 56 : 224;   // token rows per TMA box
@@ -104,7 +110,7 @@ struct Cfg {
   // SF slot: 4 weight-SF columns, then per sub-tile kSub/32 token-SF columns
   // starting every 8 columns (scale-factor TMEM addresses stay 4-column aligned)
   static constexpr int kSubSfCols = kSub / 32;
-  static constexpr int kSfCols = kBf16 ? 0 : kFp4 ? 32 : TOK <= 64 ? 8 : TOK <= 224 ? 16 : 32;
+  static constexpr int kSfCols = (kBf16 || kF32) ? 0 : kFp4 ? 32 : TOK <= 64 ? 8 : TOK <= 224 ? 16 : 32;
   static __device__ __forceinline__ int tok_sf_col(int c) { return 4 + (c / kSubSfCols) * 8 + c % kSubSfCols; }
   static constexpr int kSfBase = kAccBufs * TOK;
   static constexpr int kTmemUsed = kSfBase + kSfSlots * kSfCols;
@@ -118,7 +124,8 @@ struct Cfg {
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kStageB + kStageA) + kEpiBytes +
                                   kTableBytes + kBarBytes;
   static_assert(kSfBase + kSfSlots * kSfCols <= 512, "TMEM columns");
-  static_assert(kBf16 || 4 + (TOK / kSub - 1) * 8 + kSubSfCols <= kSfCols, "SF slot width");
+  static_assert(kBf16 || kF32 || 4 + (TOK / kSub - 1) * 8 + kSubSfCols <= kSfCols, "SF slot width");
+  static_assert(!kF32 || (TOK == 64 && CPS == 1), "FP32-scale tile: 64 tokens, one CTA per SM (register budget)");
   static_assert(kSubSfCols <= 8, "token SF columns of a sub-tile");
   static_assert(kTmemUsed <= 512, "TMEM budget");
   static_assert(kSmem * CPS + 1024 * CPS <= 233472, "shared memory budget");
@@ -314,7 +321,31 @@ __global__ void __launch_bounds__(kThreads, CPS)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (C::kF32 && lane == 0) {
+      // one partial accumulator per 128-K stage, alternating between the two TMEM buffers
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = t_first; t < total_tiles && ok; t += G) {
+        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
+        const uint32_t mma_n = (tl.ntok + 15) & ~15;
+        const uint32_t idesc = idesc_f8(kBlockW, mma_n);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t adesc = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB));
+          const uint64_t bdesc = smem_desc_k_sw128(smem_u32(stage_a + stage * C::kStageA));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_f8(tmem_base + acc * TOK, adesc + 2 * k, bdesc + 2 * k, idesc, k != 0);
+          tc_commit(&empty[stage]);
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+          tc_commit(&acc_full[acc]);
+          if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
+        }
+      }
+      tc_commit(mma_done);
+      drain_wait(mma_done, 0);
+    } else if (!C::kF32 && lane == 0) {
       uint32_t stage = 0, phase = 0, sf_slot = 0, sf_phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int t = t_first; t < total_tiles && ok; t += G) {
@@ -386,6 +417,69 @@ __global__ void __launch_bounds__(kThreads, CPS)
     const int q = warp & 3;                       // TMEM lane quadrant = weight rows 32q..32q+31
     uint16_t* buf = reinterpret_cast<uint16_t*>(epi) + (warp - 2) * 32 * 32;
     uint32_t acc = 0, acc_phase = 0;
+    if constexpr (C::kF32) {
+      // D[token, row] = sum_kb sB[e, nt, kb] * sA[token, kb] * partial_kb: promoted in FP32 registers,
+      // in K-block order; lane = weight row 32q + lane, accv[j] = token j of the tile
+      const int nnb = N / kBlockW;
+      bool ok = true;
+      for (int t = t_first; t < total_tiles && ok; t += G) {
+        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
+        float accv[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) accv[j] = 0.f;
+        const float* sbp = p.sfb_f32 + (static_cast<int64_t>(tl.e) * nnb + tl.nt) * nkb;
+        const int64_t r0 = static_cast<int64_t>(tl.tok0) + lane;
+        for (int kb = 0; kb < nkb; ++kb) {
+          const float sb = __ldg(sbp + kb);
+          const float* sap = p.sfa_f32 + static_cast<int64_t>(kb) * p.sfa_ld;
+          const float sa0 = lane < tl.ntok ? __ldg(sap + r0) : 0.f;
+          const float sa1 = lane + 32 < tl.ntok ? __ldg(sap + r0 + 32) : 0.f;
+          if (!warp_wait(&acc_full[acc], acc_phase, abort_flag, p.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * TOK;
+          uint32_t r[32];
+          tmem_ld_x32(taddr, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            accv[j] = fmaf(__uint_as_float(r[j]), sb * __shfl_sync(0xffffffffu, sa0, j), accv[j]);
+          if (tl.ntok > 32) {
+            tmem_ld_x32(taddr + 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              accv[32 + j] = fmaf(__uint_as_float(r[j]), sb * __shfl_sync(0xffffffffu, sa1, j), accv[32 + j]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int c0 = 32 * half;
+          if (c0 >= tl.ntok) break;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(accv[c0 + j]);
+            buf[j * 32 + lane] = *reinterpret_cast<const uint16_t*>(&h);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = (lane >> 2) + 8 * i;
+            if (c0 + j < tl.ntok) {
+              const uint4 v = *reinterpret_cast<const uint4*>(buf + j * 32 + (lane & 3) * 8);
+              uint16_t* dst = p.d + static_cast<int64_t>(tl.tok0 + c0 + j) * N + tl.nt * kBlockW + 32 * q +
+                              (lane & 3) * 8;
+              *reinterpret_cast<uint4*>(dst) = v;
+            }
+          }
+          __syncwarp();
+        }
+      }
+    } else
     for (int t = t_first; t < total_tiles; t += G) {
       const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
       if (!warp_wait(&acc_full[acc], acc_phase, abort_flag, p.err)) break;
@@ -442,8 +536,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
     const int q = warp & 3;
     uint32_t sf_slot = 0, sf_phase = 0;
     bool ok = true;
-    if constexpr (C::kBf16) {
-      // no scale factors
+    if constexpr (C::kBf16 || C::kF32) {
+      // no scale factors in tensor memory
     } else if constexpr (C::kFp4) {
       // NVFP4: per stage, MMA k's word of weight row (lane + 32c) -> column 4k + c, of token
       // row (lane + 32c) -> column 16 + 4k + c; rows past the tile get scale 0
@@ -811,4 +905,52 @@ extern "C" bsf_status bsf_grouped_gemm_bf16_masked(const void* a, const void* b,
   }
   const int64_t max_tiles = E * ((max_m + kBigTok - 1) / kBigTok) * (N / 128);
   return launch<kBigTok, 2, kMaxExperts, kFmtBf16>(args, ad, bd, max_tiles, s);
+}
+
+// ---------------------------------------------------------------- FP8 with float32 scales
+// "AsymGEMM" README, disable_ue8m0_cast: the scales stay float32.  They cannot
+// feed the block-scaled MMA (UE8M0 / UE4M3 only), so each 128-K stage is a
+// separate unscaled MMA (kind::f8f6f4) into a TMEM partial, and the epilogue
+// warps add sA * sB * partial in FP32 (the DeepGEMM article's software path of
+// "补偿机制二").
+
+extern "C" bsf_status bsf_grouped_gemm_f32sf_contig(const uint8_t* a, const float* sfa, int64_t sfa_ld, int64_t m_cap,
+                                                    const uint8_t* b, const float* sfb, void* d,
+                                                    const int32_t* seg_start, const int32_t* counts, int64_t E,
+                                                    int64_t N, int64_t K, int flags, bsf_stream_t stream) {
+  if (m_cap <= 0) return m_cap == 0 ? BSF_OK : BSF_ERR_INVALID_ARGUMENT;
+  const int32_t* sfa_i = reinterpret_cast<const int32_t*>(sfa);
+  const int32_t* sfb_i = reinterpret_cast<const int32_t*>(sfb);
+  bsf_status st = check_common(a, sfa_i, sfa_ld, m_cap, b, sfb_i, d, E, N, K, flags);
+  if (st != BSF_OK) return st;
+  if (!seg_start || !counts) return BSF_ERR_INVALID_ARGUMENT;
+  if ((st = resolve_b(flags, &b, &sfb_i)) != BSF_OK) return st;
+  int* err = device_error_ptr();
+  if (!err) return BSF_ERR_CUDA;
+  GemmArgs args{seg_start, counts, 0, m_cap, nullptr, sfa_ld, nullptr, static_cast<uint16_t*>(d),
+                static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
+                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0, 0, nullptr, sfa, reinterpret_cast<const float*>(sfb_i)};
+  const int64_t max_tiles = (m_cap / 64 + E) * (N / 128);
+  return launch<64, 1, kMaxExperts, kFmtFp8F32>(args, a, b, max_tiles, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" bsf_status bsf_grouped_gemm_f32sf_masked(const uint8_t* a, const float* sfa, int64_t sfa_ld,
+                                                    const uint8_t* b, const float* sfb, void* d,
+                                                    const int32_t* masked_m, int64_t E, int64_t max_m, int64_t N,
+                                                    int64_t K, int flags, bsf_stream_t stream) {
+  if (max_m <= 0) return BSF_ERR_INVALID_ARGUMENT;
+  const int64_t m_rows = E * max_m;
+  const int32_t* sfa_i = reinterpret_cast<const int32_t*>(sfa);
+  const int32_t* sfb_i = reinterpret_cast<const int32_t*>(sfb);
+  bsf_status st = check_common(a, sfa_i, sfa_ld, m_rows, b, sfb_i, d, E, N, K, flags);
+  if (st != BSF_OK) return st;
+  if (!masked_m) return BSF_ERR_INVALID_ARGUMENT;
+  if ((st = resolve_b(flags, &b, &sfb_i)) != BSF_OK) return st;
+  int* err = device_error_ptr();
+  if (!err) return BSF_ERR_CUDA;
+  GemmArgs args{nullptr, masked_m, max_m, m_rows, nullptr, sfa_ld, nullptr, static_cast<uint16_t*>(d),
+                static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
+                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0, 0, nullptr, sfa, reinterpret_cast<const float*>(sfb_i)};
+  const int64_t max_tiles = E * ((max_m + 63) / 64) * (N / 128);
+  return launch<64, 1, kMaxExperts, kFmtFp8F32>(args, a, b, max_tiles, reinterpret_cast<cudaStream_t>(stream));
 }

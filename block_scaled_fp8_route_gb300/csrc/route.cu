@@ -283,7 +283,7 @@ extern "C" size_t bsf_route_workspace_bytes(int64_t T, int64_t kr, int64_t E) {
 namespace bsf {
 namespace {
 
-enum RowFormat { kRowsFp8, kRowsNvfp4, kRowsBf16 };
+enum RowFormat { kRowsFp8, kRowsNvfp4, kRowsBf16, kRowsFp8F32 };
 
 // bsf_route / bsf_route_nvfp4 / bsf_route_bf16: fmt selects the scatter's row format
 // (FP8: K bytes + ceil(K/512) SF words; NVFP4: K/2 bytes + K/64 words; BF16: 2K bytes, no SF).
@@ -336,7 +336,8 @@ bsf_status route_impl(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E,
     route_fill_kernel<<<static_cast<unsigned>(fill_blocks), kThreads, 0, s>>>(
         e32, m_cap, counts, seg_start, token_of_row, m_indices, q, sf, sf_ld,
         fmt == kRowsNvfp4 ? K / 2 : fmt == kRowsBf16 ? 2 * K : K,
-        fmt == kRowsNvfp4 ? K / 64 : fmt == kRowsBf16 ? 0 : (K + 511) / 512, a_packed, sfa_packed, sfa_ld);
+        fmt == kRowsNvfp4 ? K / 64 : fmt == kRowsBf16 ? 0 : fmt == kRowsFp8F32 ? K / 128 : (K + 511) / 512, a_packed,
+        sfa_packed, sfa_ld);
   }
   return launch_status();
 }
@@ -363,6 +364,17 @@ extern "C" bsf_status bsf_route_nvfp4(const int32_t* topk_ids, int64_t T, int64_
   return route_impl(topk_ids, T, kr, E, layout, align_or_max_m, counts, seg_start, output_index, token_of_row,
                     m_indices, m_cap, q, sf, sf_ld, K, kRowsNvfp4, a_packed, sfa_packed, sfa_ld, workspace,
                     workspace_bytes, stream);
+}
+
+extern "C" bsf_status bsf_route_f32sf(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout,
+                                      int64_t align_or_max_m, int32_t* counts, int32_t* seg_start,
+                                      int32_t* output_index, int32_t* token_of_row, int32_t* m_indices,
+                                      int64_t m_cap, const uint8_t* q, const float* sf, int64_t sf_ld, int64_t K,
+                                      uint8_t* a_packed, float* sfa_packed, int64_t sfa_ld, void* workspace,
+                                      size_t workspace_bytes, bsf_stream_t stream) {
+  return route_impl(topk_ids, T, kr, E, layout, align_or_max_m, counts, seg_start, output_index, token_of_row,
+                    m_indices, m_cap, q, reinterpret_cast<const int32_t*>(sf), sf_ld, K, kRowsFp8F32, a_packed,
+                    reinterpret_cast<int32_t*>(sfa_packed), sfa_ld, workspace, workspace_bytes, stream);
 }
 
 extern "C" bsf_status bsf_route_bf16(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout,

@@ -105,7 +105,10 @@ class RouteBuffers:
         ws = _lib.load().bsf_route_workspace_bytes(T, kr, E)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
         self.fmt = fmt
-        if scatter and K and fmt == "bf16":
+        if scatter and K and fmt == "fp8_f32sf":
+            self.a_packed = torch.empty((max(self.m_cap, 1), K), dtype=torch.uint8, device=device)
+            self.sfa_packed = torch.empty((K // 128, sf_ld(self.m_cap)), dtype=torch.float32, device=device)
+        elif scatter and K and fmt == "bf16":
             self.a_packed = torch.empty((max(self.m_cap, 1), K), dtype=torch.bfloat16, device=device)
             self.sfa_packed = None
         elif scatter and K and fmt == "nvfp4":
@@ -135,7 +138,7 @@ def route(topk_ids, E, layout, align_or_max_m, q=None, sf=None, bufs=None, strea
             _ptr(bufs.a_packed) if q is not None else None, _ptr(bufs.workspace), bufs.workspace.numel(),
             _stream(stream)), "route_bf16")
         return bufs
-    fn = lib.bsf_route_nvfp4 if fmt == "nvfp4" else lib.bsf_route
+    fn = {"nvfp4": lib.bsf_route_nvfp4, "fp8_f32sf": lib.bsf_route_f32sf}.get(fmt, lib.bsf_route)
     _lib.check(fn(
         _ptr(topk_ids.contiguous()), T, kr, E, layout, align_or_max_m,
         _ptr(bufs.counts), _ptr(bufs.seg_start), _ptr(bufs.output_index), _ptr(bufs.token_of_row),
@@ -313,4 +316,51 @@ def grouped_gemm_bf16_masked(a, b, masked_m, max_m, d=None, expected_m=0, flags=
     _lib.check(_lib.load().bsf_grouped_gemm_bf16_masked(
         _ptr(a), _ptr(b), _ptr(d), _ptr(masked_m), E, max_m, N, K, expected_m, flags, _stream(stream)),
         "grouped_gemm_bf16_masked")
+    return d
+
+
+# ----------------------------------------------------------------------------- FP8 with float32 scales
+def quantise_act_f32sf(x, q=None, sf=None, stream=None):
+    """x bf16 [T, K] -> (q uint8 [T, K], sf float32 [K/128, sf_ld(T)])."""
+    T, K = x.shape
+    if q is None:
+        q = torch.empty((T, K), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty((K // 128, sf_ld(T)), dtype=torch.float32, device=x.device)
+    _lib.check(_lib.load().bsf_quantise_act_f32sf(_ptr(x.contiguous()), T, K, _ptr(q), _ptr(sf), sf.shape[1],
+                                                  _stream(stream)), "quantise_act_f32sf")
+    return q, sf
+
+
+def quantise_weight_f32sf(w, stream=None):
+    """w bf16 [E, N, K] -> (q uint8 [E, N, K], sf float32 [E, N/128, K/128])."""
+    E, N, K = w.shape
+    q = torch.empty((E, N, K), dtype=torch.uint8, device=w.device)
+    sf = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device=w.device)
+    _lib.check(_lib.load().bsf_quantise_weight_f32sf(_ptr(w.contiguous()), E, N, K, _ptr(q), _ptr(sf),
+                                                     _stream(stream)), "quantise_weight_f32sf")
+    return q, sf
+
+
+def grouped_gemm_f32sf_contig(a, sfa, b, sfb, seg_start, counts, d=None, flags=0, stream=None):
+    """a uint8 [m_cap, K], sfa float32 [K/128, ld], b uint8 [E, N, K], sfb float32 [E, N/128, K/128]."""
+    m_cap, K = a.shape
+    E, N, _ = b.shape
+    if d is None:
+        d = torch.empty((m_cap, N), dtype=torch.bfloat16, device=a.device)
+    _lib.check(_lib.load().bsf_grouped_gemm_f32sf_contig(
+        _ptr(a), _ptr(sfa), sfa.shape[1], m_cap, _ptr(b), _ptr(sfb), _ptr(d), _ptr(seg_start), _ptr(counts),
+        E, N, K, flags, _stream(stream)), "grouped_gemm_f32sf_contig")
+    return d
+
+
+def grouped_gemm_f32sf_masked(a, sfa, b, sfb, masked_m, max_m, d=None, flags=0, stream=None):
+    """a uint8 [E*max_m, K], sfa float32 [K/128, ld] -> d bf16 [E*max_m, N]."""
+    K = a.shape[-1]
+    E, N, _ = b.shape
+    if d is None:
+        d = torch.empty((E * max_m, N), dtype=torch.bfloat16, device=a.device)
+    _lib.check(_lib.load().bsf_grouped_gemm_f32sf_masked(
+        _ptr(a), _ptr(sfa), sfa.shape[1], _ptr(b), _ptr(sfb), _ptr(d), _ptr(masked_m), E, max_m, N, K, flags,
+        _stream(stream)), "grouped_gemm_f32sf_masked")
     return d

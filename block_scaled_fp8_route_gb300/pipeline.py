@@ -20,7 +20,8 @@ from . import ops
 class MoEPath:
     """``fmt`` = "fp8" (E4M3, UE8M0 per 1 x 128 / 128 x 128), "nvfp4" (E2M1, UE4M3 per 1 x 16, a
     power-of-two tensor exponent per expert for the weights and ``a_exp`` for the activations) or
-    "bf16" (unquantised operands; the route scatters bf16 rows)."""
+    "bf16" (unquantised operands; the route scatters bf16 rows) or "fp8_f32sf" (E4M3 with float32
+    scales, applied per 128-K block in software)."""
 
     def __init__(self, E, kr, T, K, N, w_bf16, layout=ops.CONTIGUOUS, align_or_max_m=1, w2_bf16=None,
                  device="cuda", weights_on_host=False, expected_m=0, fused_dispatch=None, fmt="fp8", a_exp=0):
@@ -39,8 +40,8 @@ class MoEPath:
             self.w2q, self.sfb2, self.b2_exp = self._weights(w2_bf16.to(device), self.K2)
         self.bufs = ops.RouteBuffers(T, kr, E, layout, align_or_max_m, K=K, device=device, fmt=fmt)
         self.fused_dispatch = ops.dispatch_supported(T, kr, E) if fused_dispatch is None else fused_dispatch
-        if fmt == "bf16":
-            self.fused_dispatch = False          # nothing to quantise: the route scatters the bf16 rows
+        if fmt in ("bf16", "fp8_f32sf"):
+            self.fused_dispatch = False          # the route scatters the rows (bf16, or e4m3 + float32 scales)
         m = self.bufs.m_cap
         self.q, self.sf = self._act_buffers(T, K, device)
         self.y = torch.empty((max(m, 1), N), dtype=torch.bfloat16, device=device)
@@ -54,6 +55,9 @@ class MoEPath:
     def _weights(self, w, K):
         if self.fmt == "bf16":
             return w.contiguous(), None, None
+        if self.fmt == "fp8_f32sf":
+            wq, sf = ops.quantise_weight_f32sf(w)
+            return wq, sf, None
         if self.fmt == "nvfp4":
             return ops.quantise_weight_nvfp4(w)
         wq, sf128 = ops.quantise_weight(w)
@@ -62,6 +66,9 @@ class MoEPath:
     def _act_buffers(self, rows, K, device):
         if self.fmt == "bf16":
             return None, None
+        if self.fmt == "fp8_f32sf":
+            return (torch.empty((rows, K), dtype=torch.uint8, device=device),
+                    torch.empty((K // 128, ops.sf_ld(rows)), dtype=torch.float32, device=device))
         if self.fmt == "nvfp4":
             return (torch.empty((rows, K // 2), dtype=torch.uint8, device=device),
                     torch.empty((K // 64, ops.sf_ld(rows)), dtype=torch.int32, device=device))
@@ -69,6 +76,8 @@ class MoEPath:
                 torch.empty((ops.sf_words(K), ops.sf_ld(rows)), dtype=torch.int32, device=device))
 
     def _quantise(self, x, q, sf):
+        if self.fmt == "fp8_f32sf":
+            return ops.quantise_act_f32sf(x, q=q, sf=sf)
         if self.fmt == "nvfp4":
             return ops.quantise_act_nvfp4(x, self.a_exp, q=q, sf=sf)
         return ops.quantise_act(x, q=q, sf=sf)
@@ -93,6 +102,11 @@ class MoEPath:
                 return ops.grouped_gemm_bf16_masked(a, wq, b.counts, self.align_or_max_m, d=d,
                                                     expected_m=self.expected_m, flags=self.flags)
             return ops.grouped_gemm_bf16_contig(a, wq, b.seg_start, b.counts, d=d, flags=self.flags)
+        if self.fmt == "fp8_f32sf":
+            if self.layout == ops.MASKED:
+                return ops.grouped_gemm_f32sf_masked(a, sfa, wq, sfb, b.counts, self.align_or_max_m, d=d,
+                                                     flags=self.flags)
+            return ops.grouped_gemm_f32sf_contig(a, sfa, wq, sfb, b.seg_start, b.counts, d=d, flags=self.flags)
         if self.fmt == "nvfp4":
             if self.layout == ops.MASKED:
                 return ops.grouped_gemm_nvfp4_masked(a, sfa, self.a_exp, wq, sfb, b_exp, b.counts,

@@ -387,6 +387,50 @@ bsf_status bsf_grouped_gemm_bf16_masked(const void* a, const void* b, void* d, c
                                         int64_t max_m, int64_t N, int64_t K, int64_t expected_m, int flags,
                                         bsf_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * FP8 E4M3 with float32 scale factors ("AsymGEMM" README, notation:
+ * disable_ue8m0_cast keeps the scale factors in float32 rather than UE8M0).
+ * Per block (1 x 128 along K for activations, 128 x 128 for weights):
+ * s = amax / 448 (one float32 division, nearest even; 1 for an all-zero
+ * block), q = E4M3(x / s) (one float32 division, nearest-even E4M3,
+ * saturating).  Scales: activations float32 [K/128][sf_ld] (MN-major,
+ * sf_ld >= rows, multiple of 4); weights float32 [E][N/128][K/128].
+ */
+
+/* bsf_quantise_act_f32sf — x bf16 [T, K] (K % 128 == 0) -> q e4m3 [T, K], sf float32 [K/128][sf_ld]. */
+bsf_status bsf_quantise_act_f32sf(const void* x, int64_t T, int64_t K, uint8_t* q, float* sf, int64_t sf_ld,
+                                  bsf_stream_t stream);
+
+/* bsf_quantise_weight_f32sf — w bf16 [E, N, K] -> q e4m3 [E, N, K], sf float32 [E][N/128][K/128]. */
+bsf_status bsf_quantise_weight_f32sf(const void* w, int64_t E, int64_t N, int64_t K, uint8_t* q, float* sf,
+                                     bsf_stream_t stream);
+
+/* bsf_route_f32sf — bsf_route whose scatter copies e4m3 rows with their
+ * float32 scale columns (q [T, K], sf [K/128][sf_ld] -> a_packed [m_cap, K],
+ * sfa_packed [K/128][sfa_ld]).  Everything else as in bsf_route. */
+bsf_status bsf_route_f32sf(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, int layout,
+                           int64_t align_or_max_m, int32_t* counts, int32_t* seg_start, int32_t* output_index,
+                           int32_t* token_of_row, int32_t* m_indices, int64_t m_cap, const uint8_t* q,
+                           const float* sf, int64_t sf_ld, int64_t K, uint8_t* a_packed, float* sfa_packed,
+                           int64_t sfa_ld, void* workspace, size_t workspace_bytes, bsf_stream_t stream);
+
+/* bsf_grouped_gemm_f32sf_contig / _masked — D[r, n] = BF16( sum_kb sA[r, kb]
+ * sB_e[n/128, kb] sum_{k in kb} A[r, k] B_e[n, k] ) over 128-wide K-blocks
+ * kb: every block is an unscaled FP8 MMA into its own FP32 partial (tensor
+ * memory), then scaled and added in FP32 in K-block order on the CUDA cores.
+ * Tiles of up to 64 tokens, one CTA per SM (an expert with more rows is
+ * split into 64-row chunks, each streaming the expert's weights).  Needs
+ * N % 128 == 0, K % 128 == 0, 16-byte aligned a, b, d, sfa.  Segments,
+ * masks, flags (BSF_B_HOST_MAPPED: b and sfb pinned host memory), launch
+ * order and errors as in the UE8M0 calls. */
+bsf_status bsf_grouped_gemm_f32sf_contig(const uint8_t* a, const float* sfa, int64_t sfa_ld, int64_t m_cap,
+                                         const uint8_t* b, const float* sfb, void* d, const int32_t* seg_start,
+                                         const int32_t* counts, int64_t E, int64_t N, int64_t K, int flags,
+                                         bsf_stream_t stream);
+bsf_status bsf_grouped_gemm_f32sf_masked(const uint8_t* a, const float* sfa, int64_t sfa_ld, const uint8_t* b,
+                                         const float* sfb, void* d, const int32_t* masked_m, int64_t E,
+                                         int64_t max_m, int64_t N, int64_t K, int flags, bsf_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
