@@ -92,8 +92,15 @@ struct Cfg {
   static constexpr int kMaxE = MAXE;
   static constexpr int kKElems = kFp4 ? 256 : kBf16 ? 64 : 128;   // K values per stage
   static constexpr int kKbPerSlot = kFp4 ? 1 : 4;            // stages per SF slot
-  static constexpr int kStages = CPS == 2 ? (TOK <= 64 ? (MAXE <= 256 ? 4 : 3) : TOK <= 128 ? 3 : 2)
-                                          : TOK <= 64 ? 8 : TOK <= 224 ? 4 : 2;
+  // NVFP4 stages also carry the stage's scale words (TMA), which costs one stage of ring depth
+  static constexpr int kStages = kFp4 ? (TOK <= 64 ? 3 : 2)
+                                      : CPS == 2 ? (TOK <= 64 ? (MAXE <= 256 ? 4 : 3) : TOK <= 128 ? 3 : 2)
+                                                 : TOK <= 64 ? 8 : TOK <= 224 ? 4 : 2;
+  // NVFP4 scale words of one stage in shared memory: weights [4 MMAs][128 rows] int32 (box 128 x 4),
+  // tokens [4 MMAs][TOK + 4] int32 (box TOK + 4 wide from the 4-aligned row at or below the tile's first)
+  static constexpr int kSfTokCols = TOK + 4;
+  static constexpr int kSfStageBytes = kFp4 ? 4 * kBlockW * 4 + 4 * kSfTokCols * 4 : 0;
+  static constexpr int kStageSf = (kSfStageBytes + 127) / 128 * 128;
   static constexpr int kAccBufs = (kF32 || (CPS == 1 && TOK <= 224)) ? 2 : 1;
   static constexpr int kSfSlots = kFp4 ? 4 : (CPS == 1 && TOK <= 224) ? 4 : 2;
   static constexpr int kTokSfCols = (TOK + 31) / 32;
@@ -121,8 +128,8 @@ struct Cfg {
   static constexpr int kEpiBytes = 4 * 32 * 32 * 2;           // per epilogue warp: 32 tokens x 32 columns bf16
   static constexpr int kTableBytes = (3 * MAXE + 4) * 4;
   static constexpr int kBarBytes = 256;
-  static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kStageB + kStageA) + kEpiBytes +
-                                  kTableBytes + kBarBytes;
+  static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kStageB + kStageA + kStageSf) +
+                                  kEpiBytes + kTableBytes + kBarBytes;
   static_assert(kSfBase + kSfSlots * kSfCols <= 512, "TMEM columns");
   static_assert(kBf16 || kF32 || 4 + (TOK / kSub - 1) * 8 + kSubSfCols <= kSfCols, "SF slot width");
   static_assert(!kF32 || (TOK == 64 && CPS == 1), "FP32-scale tile: 64 tokens, one CTA per SM (register budget)");
@@ -187,13 +194,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 template <int TOK, int CPS, int MAXE, int FMT>
 __global__ void __launch_bounds__(kThreads, CPS)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_a,
+                        const __grid_constant__ CUtensorMap tmap_sfb, const __grid_constant__ CUtensorMap tmap_sfa,
                         const GemmArgs p) {
   using C = Cfg<TOK, CPS, MAXE, FMT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_b = smem;
   uint8_t* stage_a = stage_b + C::kStages * C::kStageB;
-  uint8_t* epi = stage_a + C::kStages * C::kStageA;
+  uint8_t* stage_sf = stage_a + C::kStages * C::kStageA;    // NVFP4 only (kStageSf = 0 otherwise)
+  uint8_t* epi = stage_sf + C::kStages * C::kStageSf;
   int* tile_start = reinterpret_cast<int*>(epi + C::kEpiBytes);
   int* exp_row0 = tile_start + C::kMaxE + 1;
   int* exp_cnt = exp_row0 + C::kMaxE;
@@ -218,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], C::kFp4 ? 5 : 1);      // NVFP4: the MMA commit and the four SF warps
     }
     for (int s = 0; s < C::kSfSlots; ++s) {
       mbar_init(&sf_full[s], 4);
@@ -233,6 +242,10 @@ __global__ void __launch_bounds__(kThreads, CPS)
     fence_barrier_init();
     tma_prefetch_desc(&tmap_b);
     tma_prefetch_desc(&tmap_a);
+    if (C::kFp4) {
+      tma_prefetch_desc(&tmap_sfb);
+      tma_prefetch_desc(&tmap_sfa);
+    }
   }
   // when launched as a dependent, everything above overlaps the tail of the preceding kernel;
   // no global memory and no tensor memory is touched before it has completed (no-op otherwise)
@@ -298,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
       for (int t = t_first; t < total_tiles && ok; t += G) {
         const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
         const int n_loads = (tl.ntok + C::kBoxRows - 1) / C::kBoxRows;
-        const uint32_t bytes = C::kStageB + n_loads * C::kBoxRows * kBlockK;
+        const uint32_t bytes = C::kStageB + n_loads * C::kBoxRows * kBlockK + C::kSfStageBytes;
         const int wrow = tl.e * N + tl.nt * kBlockW;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
@@ -307,6 +320,13 @@ __global__ void __launch_bounds__(kThreads, CPS)
           for (int i = 0; i < n_loads; ++i)
             tma_load_2d(stage_a + stage * C::kStageA + i * C::kBoxRows * kBlockK, &tmap_a, &full[stage],
                         kb * kBlockK, tl.tok0 + i * C::kBoxRows);
+          if (C::kFp4) {
+            // scale words of MMAs 4kb .. 4kb+3: weight rows of the tile, and the tile's token rows
+            // from the 4-aligned row at or below tok0 (the x coordinate of a TMA copy must be 16-byte aligned)
+            uint8_t* sf_dst = stage_sf + stage * C::kStageSf;
+            tma_load_2d(sf_dst, &tmap_sfb, &full[stage], tl.nt * kBlockW, tl.e * nw + kb * 4);
+            tma_load_2d(sf_dst + 4 * kBlockW * 4, &tmap_sfa, &full[stage], tl.tok0 & ~3, kb * 4);
+          }
           ++issued;
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
@@ -539,28 +559,33 @@ __global__ void __launch_bounds__(kThreads, CPS)
     if constexpr (C::kBf16 || C::kF32) {
       // no scale factors in tensor memory
     } else if constexpr (C::kFp4) {
-      // NVFP4: per stage, MMA k's word of weight row (lane + 32c) -> column 4k + c, of token
-      // row (lane + 32c) -> column 16 + 4k + c; rows past the tile get scale 0
+      // NVFP4: the stage's scale words arrive with its data (TMA into shared memory); per stage,
+      // MMA k's word of weight row (lane + 32c) -> TMEM column 4k + c, of token row (lane + 32c)
+      // -> column 16 + 4k + c (rows past the tile: scale 0).  The shared-memory stage is released
+      // (one of the five arrivals on its empty barrier) as soon as the words are in registers.
+      uint32_t stage = 0, phase = 0;
       for (int t = t_first; t < total_tiles && ok; t += G) {
         const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
-        const int mma_n = (tl.ntok + 15) & ~15;
-        const int32_t* sfb_base = p.sfb + static_cast<int64_t>(tl.e) * nw * N + tl.nt * kBlockW + lane;
+        const int off = tl.tok0 & 3;
         for (int kb = 0; kb < nkb; ++kb) {
+          if (!warp_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+          const uint32_t* sw = reinterpret_cast<const uint32_t*>(stage_sf + stage * C::kStageSf);
+          const uint32_t* st = sw + 4 * kBlockW;
           uint32_t w[4][4];
           uint32_t a[4][C::kTokSfCols];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const int64_t word = static_cast<int64_t>(kb) * 4 + k;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) w[k][c] = static_cast<uint32_t>(__ldg(sfb_base + word * N + 32 * c));
+            for (int c = 0; c < 4; ++c) w[k][c] = sw[k * kBlockW + 32 * c + lane];
 #pragma unroll
             for (int c = 0; c < C::kTokSfCols; ++c) {
               const int rl = lane + 32 * c;
-              const int64_t row = static_cast<int64_t>(tl.tok0) + rl;
-              a[k][c] = (rl < mma_n && row < p.m_rows) ? static_cast<uint32_t>(__ldg(p.sfa + word * p.sfa_ld + row))
-                                                       : 0u;
+              a[k][c] = rl < tl.ntok ? st[k * C::kSfTokCols + off + rl] : 0u;
             }
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[stage]);
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
           if (!warp_wait(&sf_empty[sf_slot], sf_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t col =
@@ -634,6 +659,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D uint8 tensor [rows, cols] (row pitch = cols bytes), box {128 cols, box_rows}, 128-byte swizzle.
+// 2-D int32 tensor [rows, cols] (row pitch = cols words), box {box_cols, box_rows}, no swizzle;
+// reads past the edges fill zeros.  Scale words of the NVFP4 stages.
+bool make_map_i32(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, uint32_t box_cols,
+                  uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -654,6 +694,12 @@ bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int6
   const int64_t row_bytes = C::kFp4 ? args.K / 2 : C::kBf16 ? 2 * args.K : args.K;
   if (!make_map(&map_a, a, args.m_rows, row_bytes, C::kBoxRows)) return BSF_ERR_CUDA;
   if (!make_map(&map_b, b, static_cast<int64_t>(args.E) * args.N, row_bytes, kBlockW)) return BSF_ERR_CUDA;
+  CUtensorMap map_sfb = map_b, map_sfa = map_a;     // placeholders: only NVFP4 stages load scale words by TMA
+  if (C::kFp4) {
+    const int64_t nw = args.K / 64;
+    if (!make_map_i32(&map_sfb, args.sfb, static_cast<int64_t>(args.E) * nw, args.N, kBlockW, 4)) return BSF_ERR_CUDA;
+    if (!make_map_i32(&map_sfa, args.sfa, nw, args.sfa_ld, C::kSfTokCols, 4)) return BSF_ERR_CUDA;
+  }
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -672,8 +718,9 @@ bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int6
   if (grid <= 0) return BSF_OK;
   if (C::kDependentLaunch)
     return launch_dependent(grouped_gemm_kernel<TOK, CPS, MAXE, FMT>, static_cast<unsigned>(grid), kThreads, C::kSmem, s,
-                            map_b, map_a, args);
-  grouped_gemm_kernel<TOK, CPS, MAXE, FMT><<<static_cast<unsigned>(grid), kThreads, C::kSmem, s>>>(map_b, map_a, args);
+                            map_b, map_a, map_sfb, map_sfa, args);
+  grouped_gemm_kernel<TOK, CPS, MAXE, FMT><<<static_cast<unsigned>(grid), kThreads, C::kSmem, s>>>(
+      map_b, map_a, map_sfb, map_sfa, args);
   return launch_status();
 }
 
