@@ -101,8 +101,8 @@ struct Cfg {
   static constexpr int kSfTokCols = TOK + 4;
   static constexpr int kSfStageBytes = kFp4 ? 4 * kBlockW * 4 + 4 * kSfTokCols * 4 : 0;
   static constexpr int kStageSf = (kSfStageBytes + 127) / 128 * 128;
-  static constexpr int kAccBufs = (kF32 || (CPS == 1 && TOK <= 224)) ? 2 : 1;
-  static constexpr int kSfSlots = kFp4 ? 4 : (CPS == 1 && TOK <= 224) ? 4 : 2;
+  static constexpr int kAccBufs = kF32 ? 4 : (CPS == 1 && TOK <= 224) ? 2 : 1;
+  static constexpr int kSfSlots = (kBf16 || kF32) ? 1 : kFp4 ? 4 : (CPS == 1 && TOK <= 224) ? 4 : 2;
   static constexpr int kTokSfCols = (TOK + 31) / 32;
   static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK <= 128 ? 64 : TOK <= 224 ? 56 : 224;   // token rows per TMA box
   // Launched as a programmatic dependent of the preceding kernel (dispatch / route / quantise)
@@ -127,7 +127,10 @@ struct Cfg {
   static constexpr int kStageA = TOK * kBlockK;
   static constexpr int kEpiBytes = 4 * 32 * 32 * 2;           // per epilogue warp: 32 tokens x 32 columns bf16
   static constexpr int kTableBytes = (3 * MAXE + 4) * 4;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
+  // full + empty per stage, sf_full + sf_empty per SF slot, acc_full + acc_empty per accumulator,
+  // mma_done; then the TMEM base word and the abort flag
+  static_assert((2 * kStages + 2 * kSfSlots + 2 * kAccBufs + 1) * 8 + 8 <= kBarBytes, "barrier region");
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kStageB + kStageA + kStageSf) +
                                   kEpiBytes + kTableBytes + kBarBytes;
   static_assert(kSfBase + kSfSlots * kSfCols <= 512, "TMEM columns");
@@ -449,11 +452,28 @@ __global__ void __launch_bounds__(kThreads, CPS)
         for (int j = 0; j < 64; ++j) accv[j] = 0.f;
         const float* sbp = p.sfb_f32 + (static_cast<int64_t>(tl.e) * nnb + tl.nt) * nkb;
         const int64_t r0 = static_cast<int64_t>(tl.tok0) + lane;
+        // the scales of K-blocks kb .. kb+3 are in flight ahead of their partials (a queue in registers)
+        float qb[4], q0[4], q1[4];
+        auto fetch = [&](int kk, float& b, float& s0, float& s1) {
+          b = s0 = s1 = 0.f;
+          if (kk < nkb) {
+            const float* sap = p.sfa_f32 + static_cast<int64_t>(kk) * p.sfa_ld;
+            b = __ldg(sbp + kk);
+            if (lane < tl.ntok) s0 = __ldg(sap + r0);
+            if (lane + 32 < tl.ntok) s1 = __ldg(sap + r0 + 32);
+          }
+        };
+#pragma unroll
+        for (int i = 0; i < 4; ++i) fetch(i, qb[i], q0[i], q1[i]);
         for (int kb = 0; kb < nkb; ++kb) {
-          const float sb = __ldg(sbp + kb);
-          const float* sap = p.sfa_f32 + static_cast<int64_t>(kb) * p.sfa_ld;
-          const float sa0 = lane < tl.ntok ? __ldg(sap + r0) : 0.f;
-          const float sa1 = lane + 32 < tl.ntok ? __ldg(sap + r0 + 32) : 0.f;
+          const float sb = qb[0], sa0 = q0[0], sa1 = q1[0];
+#pragma unroll
+          for (int i = 0; i < 3; ++i) {
+            qb[i] = qb[i + 1];
+            q0[i] = q0[i + 1];
+            q1[i] = q1[i + 1];
+          }
+          fetch(kb + 4, qb[3], q0[3], q1[3]);
           if (!warp_wait(&acc_full[acc], acc_phase, abort_flag, p.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * TOK;
