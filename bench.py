@@ -43,6 +43,8 @@ def parse():
                     help="token counts of the host-weight sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-formats", action="store_true",
+                    help="skip the decode step in the other operand formats (default decode run)")
     ap.add_argument("--fmt", default="fp8", choices=["fp8", "nvfp4", "bf16", "fp8_f32sf"],
                     help="operand format: FP8 E4M3 with UE8M0 scales, NVFP4 (E2M1, UE4M3 per 16), BF16, "
                          "or FP8 with float32 scales")
@@ -568,6 +570,66 @@ def large_m_gemms(dev, pk, reps=10):
     return out
 
 
+def decode_formats(dev, pk, steps=50):
+    """The decode step in the other operand formats (NVFP4, BF16, FP8 with float32 scales): the
+    grouped GEMM timed alone over eager steps (CUDA events around its launch) and the whole step as
+    CUDA-graph replays, bytes from each format's own accounting."""
+    from block_scaled_fp8_route_gb300 import MoEPath
+    w = W.WORKLOADS["decode"]
+    ids, p = W.routing(w, device=dev)
+    x = W.activations(w, device=dev)
+    out = {}
+    for fmt in ("nvfp4", "bf16", "fp8_f32sf"):
+        wt = W.weights(w, device=dev)
+        path = MoEPath(w.E, w.kr, w.T, w.K, w.N, wt, layout=w.layout, align_or_max_m=w.max_m, device=dev,
+                       expected_m=w.T * w.kr // w.E, fmt=fmt)
+        del wt
+        torch.cuda.empty_cache()
+        path.step(x, ids, p)
+        torch.cuda.synchronize()
+        counts = path.bufs.counts.cpu().numpy()
+        placed = int(path.bufs.seg_start[-1].item())
+        byts, _ = step_work(w, counts, placed, fused_dispatch=path.fused_dispatch, fmt=fmt)
+        ev = []
+        orig = path.gemm
+
+        def timed(*a, **k):
+            e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+            e0.record()
+            r = orig(*a, **k)
+            e1.record()
+            ev.append((e0, e1))
+            return r
+
+        path.gemm = timed
+        for _ in range(steps):
+            path.step(x, ids, p)
+        torch.cuda.synchronize()
+        path.gemm = orig
+        gemm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[3:])
+        path.capture(x, ids, p)
+        for _ in range(3):
+            path.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+        e0.record()
+        for _ in range(steps):
+            path.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        step_ms = e0.elapsed_time(e1) / steps
+        from block_scaled_fp8_route_gb300 import ops
+        assert ops.device_error() == 0
+        gbs = byts["gemm"] / (gemm_ms / 1e3) / 1e9
+        out[fmt] = {"gemm_ms": gemm_ms, "gemm_gbs": gbs, "gemm_frac": gbs / pk["hbm_gbs"],
+                    "gemm_bytes": byts["gemm"], "step_ms": step_ms,
+                    "step_gbs": sum(byts.values()) / (step_ms / 1e3) / 1e9, "dtype": DTYPES[fmt]}
+        del path
+        torch.cuda.empty_cache()
+    out["peak_gbs"] = pk["hbm_gbs"]
+    return out
+
+
 # ----------------------------------------------------------------------------- GPU leg
 def main():
     args = parse()
@@ -749,6 +811,13 @@ def main():
         del probe
         torch.cuda.empty_cache()
 
+    formats = None
+    if rank == 0 and world == 1 and w.name == "decode" and args.fmt == "fp8" and not args.no_formats:
+        del path
+        torch.cuda.empty_cache()
+        path = None
+        formats = decode_formats(dev, pk)
+
     large_m = None
     if rank == 0 and world == 1 and w.name == "decode" and args.fmt == "fp8" and not args.no_large_m:
         del path
@@ -768,6 +837,7 @@ def main():
             "large_m_gemm": large_m if large_m is not None else None,
             "per_kernel_bytes": bytes_by_kernel,
             "hbm_stream_read_gbs": hbm_read,
+            "decode_formats": formats,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
