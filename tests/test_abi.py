@@ -46,6 +46,17 @@ def test_argument_validation_needs_no_device(lib):
     assert lib.bsf_dispatch(nul, 4096, 128, nul, 8, 128, 0, 1, nul, nul, nul, nul, nul, 1 << 20, nul, nul, 1 << 20,
                             nul) == 3
     assert lib.bsf_dispatch(nul, 4, 100, nul, 2, 4, 0, 1, nul, nul, nul, nul, nul, 8, nul, nul, 8, nul) == 1
+    # NVFP4: K must be a multiple of 256 for the GEMM, of 64 for the quantiser; tensor exponent within +-100
+    assert lib.bsf_grouped_gemm_nvfp4_masked(nul, nul, 64, 0, nul, nul, nul, nul, nul, 2, 32, 128, 128, 0, 0,
+                                             nul) == 1
+    assert lib.bsf_quantise_act_nvfp4(nul, 4, 96, 0, nul, nul, 4, nul) == 1
+    assert lib.bsf_quantise_act_nvfp4(nul, 4, 128, 101, nul, nul, 4, nul) == 1
+    assert lib.bsf_grouped_gemm_nvfp4_contig(nul, nul, 8, 8, 0, nul, nul, nul, nul, nul, nul, 300, 128, 256, 0,
+                                             nul) == 3                      # more than 256 experts
+    # BF16: K must be a multiple of 64
+    assert lib.bsf_grouped_gemm_bf16_contig(nul, 8, nul, nul, nul, nul, 2, 128, 96, 0, nul) == 1
+    # FP32 scales: N must be a multiple of 128
+    assert lib.bsf_grouped_gemm_f32sf_masked(nul, nul, 8, nul, nul, nul, nul, 2, 4, 100, 128, 0, nul) == 1
 
 
 def test_python_constants_match_header():
