@@ -46,7 +46,8 @@ SIGNATURES = {
                                  _p, _p, _i64, _i64, _p, _p, _i64, _p, _size, _p]),
     "bsf_grouped_gemm_f32sf_contig": (_c_int, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p, _i64, _i64, _i64, _c_int,
                                                _p]),
-    "bsf_grouped_gemm_f32sf_masked": (_c_int, [_p, _p, _i64, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _c_int, _p]),
+    "bsf_grouped_gemm_f32sf_masked": (_c_int, [_p, _p, _i64, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _c_int,
+                                               _p]),
     "bsf_nvfp4_tensor_exponent": (_c_int, [_p, _i64, _i64, _p, _p]),
     "bsf_quantise_act_nvfp4": (_c_int, [_p, _i64, _i64, _c_int, _p, _p, _i64, _p]),
     "bsf_quantise_weight_nvfp4": (_c_int, [_p, _i64, _i64, _i64, _p, _p, _p, _p]),

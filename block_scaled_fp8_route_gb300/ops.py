@@ -354,13 +354,13 @@ def grouped_gemm_f32sf_contig(a, sfa, b, sfb, seg_start, counts, d=None, flags=0
     return d
 
 
-def grouped_gemm_f32sf_masked(a, sfa, b, sfb, masked_m, max_m, d=None, flags=0, stream=None):
+def grouped_gemm_f32sf_masked(a, sfa, b, sfb, masked_m, max_m, d=None, expected_m=0, flags=0, stream=None):
     """a uint8 [E*max_m, K], sfa float32 [K/128, ld] -> d bf16 [E*max_m, N]."""
     K = a.shape[-1]
     E, N, _ = b.shape
     if d is None:
         d = torch.empty((E * max_m, N), dtype=torch.bfloat16, device=a.device)
     _lib.check(_lib.load().bsf_grouped_gemm_f32sf_masked(
-        _ptr(a), _ptr(sfa), sfa.shape[1], _ptr(b), _ptr(sfb), _ptr(d), _ptr(masked_m), E, max_m, N, K, flags,
-        _stream(stream)), "grouped_gemm_f32sf_masked")
+        _ptr(a), _ptr(sfa), sfa.shape[1], _ptr(b), _ptr(sfb), _ptr(d), _ptr(masked_m), E, max_m, N, K, expected_m,
+        flags, _stream(stream)), "grouped_gemm_f32sf_masked")
     return d

@@ -105,7 +105,7 @@ class MoEPath:
         if self.fmt == "fp8_f32sf":
             if self.layout == ops.MASKED:
                 return ops.grouped_gemm_f32sf_masked(a, sfa, wq, sfb, b.counts, self.align_or_max_m, d=d,
-                                                     flags=self.flags)
+                                                     expected_m=self.expected_m, flags=self.flags)
             return ops.grouped_gemm_f32sf_contig(a, sfa, wq, sfb, b.seg_start, b.counts, d=d, flags=self.flags)
         if self.fmt == "nvfp4":
             if self.layout == ops.MASKED:

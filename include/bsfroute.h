@@ -418,8 +418,10 @@ bsf_status bsf_route_f32sf(const int32_t* topk_ids, int64_t T, int64_t kr, int64
  * sB_e[n/128, kb] sum_{k in kb} A[r, k] B_e[n, k] ) over 128-wide K-blocks
  * kb: every block is an unscaled FP8 MMA into its own FP32 partial (tensor
  * memory), then scaled and added in FP32 in K-block order on the CUDA cores.
- * Tiles of up to 64 tokens, one CTA per SM (an expert with more rows is
- * split into 64-row chunks, each streaming the expert's weights).  Needs
+ * Tiles of up to 64 tokens with one CTA per SM, or, for masked calls with
+ * max_m <= 32 or expected_m <= 16 (a hint; 0 = unknown), of up to 32 tokens
+ * with two CTAs per SM; an expert with more rows is split into chunks, each
+ * streaming the expert's weights.  Needs
  * N % 128 == 0, K % 128 == 0, 16-byte aligned a, b, d, sfa.  Segments,
  * masks, flags (BSF_B_HOST_MAPPED: b and sfb pinned host memory), launch
  * order and errors as in the UE8M0 calls. */
@@ -429,7 +431,8 @@ bsf_status bsf_grouped_gemm_f32sf_contig(const uint8_t* a, const float* sfa, int
                                          bsf_stream_t stream);
 bsf_status bsf_grouped_gemm_f32sf_masked(const uint8_t* a, const float* sfa, int64_t sfa_ld, const uint8_t* b,
                                          const float* sfb, void* d, const int32_t* masked_m, int64_t E,
-                                         int64_t max_m, int64_t N, int64_t K, int flags, bsf_stream_t stream);
+                                         int64_t max_m, int64_t N, int64_t K, int64_t expected_m, int flags,
+                                         bsf_stream_t stream);
 
 #ifdef __cplusplus
 }

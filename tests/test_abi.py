@@ -56,7 +56,7 @@ def test_argument_validation_needs_no_device(lib):
     # BF16: K must be a multiple of 64
     assert lib.bsf_grouped_gemm_bf16_contig(nul, 8, nul, nul, nul, nul, 2, 128, 96, 0, nul) == 1
     # FP32 scales: N must be a multiple of 128
-    assert lib.bsf_grouped_gemm_f32sf_masked(nul, nul, 8, nul, nul, nul, nul, 2, 4, 100, 128, 0, nul) == 1
+    assert lib.bsf_grouped_gemm_f32sf_masked(nul, nul, 8, nul, nul, nul, nul, 2, 4, 100, 128, 0, 0, nul) == 1
 
 
 def test_python_constants_match_header():

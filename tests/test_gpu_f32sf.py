@@ -61,8 +61,8 @@ def _check(d, ref, seg, counts, what):
             check_expert_block(dg[s:s + c], ref[s:s + c], f"{what} expert {e} ({c} rows)")
 
 
-@pytest.mark.parametrize("max_m", [64, 200])
-def test_masked(dev, max_m):
+@pytest.mark.parametrize("max_m,expected_m", [(64, 0), (64, 8), (32, 0), (200, 0), (200, 8)])
+def test_masked(dev, max_m, expected_m):
     masked = np.minimum(np.array([0, 1, 16, 63, 64, max_m // 2, max_m, 7]), max_m)
     E, N, K = len(masked), 256, 512
     x, w = _x(E * max_m, K, 10 + max_m), _w(E, N, K, 11 + max_m)
@@ -70,11 +70,11 @@ def test_masked(dev, max_m):
     bq, bsf = ops.quantise_weight_f32sf(w.to(dev))
     d = torch.full((E * max_m, N), float("nan"), dtype=torch.bfloat16, device=dev)
     ops.grouped_gemm_f32sf_masked(aq, asf, bq, bsf, torch.as_tensor(masked, dtype=torch.int32, device=dev), max_m,
-                                  d=d)
+                                  d=d, expected_m=expected_m)
     torch.cuda.synchronize()
     assert ops.device_error() == 0
     seg = np.arange(E + 1) * max_m
-    _check(d, _ref(x, w, seg, masked), seg, masked, f"f32sf masked max_m={max_m}")
+    _check(d, _ref(x, w, seg, masked), seg, masked, f"f32sf masked max_m={max_m} expected_m={expected_m}")
 
 
 @pytest.mark.parametrize("align", [1, 128])
