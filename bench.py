@@ -519,6 +519,7 @@ def large_m_gemms(dev, pk, reps=10):
         ids, _ = W.routing(w, device=dev)
         bufs = ops.route(ids, w.E, w.layout, w.align)
         rows = int(bufs.counts.sum().item())
+        active = int((bufs.counts > 0).sum().item())
         res = {}
         for tag, (K, N) in enumerate(((w.K, w.N), (w.K2, w.N2))):
             x = W.activations(W.with_tokens(w, bufs.m_cap), device=dev, K=K, tag=tag)
@@ -540,7 +541,12 @@ def large_m_gemms(dev, pk, reps=10):
             torch.cuda.synchronize()
             ms = e0.elapsed_time(e1) / reps
             tf = 2.0 * rows * N * K / (ms / 1e3) / 1e12
-            res["gate_up" if tag == 0 else "down"] = {"K": K, "N": N, "ms": ms, "tflops": tf, "frac": tf / fp8_peak}
+            qb, sb = operand_bytes(K, "fp8")
+            nbytes = active * weight_bytes(N, K, "fp8") + rows * (qb + sb + 2 * N)
+            rf = binding_roofline(2.0 * rows * N * K, nbytes, ms, fp8_peak, pk["hbm_gbs"])
+            res["gate_up" if tag == 0 else "down"] = {"K": K, "N": N, "ms": ms, "tflops": tf, "frac": tf / fp8_peak,
+                                                      "bytes": nbytes, "bound": rf["bound"],
+                                                      "roofline_frac": rf["roofline_frac"]}
             del aq, asf, bq, sf128, sfb, d
             torch.cuda.empty_cache()
         out[name] = {"routed_rows": rows, **res}
@@ -568,6 +574,23 @@ def large_m_gemms(dev, pk, reps=10):
         out["library_fp8_8192_tflops"] = None
         out["library_fp8_note"] = str(exc)[:120]
     return out
+
+
+def binding_roofline(flops, nbytes, ms, tensor_peak_tflops, hbm_peak_gbs):
+    """The roofline a launch sits under: t_F = flops / tensor peak against t_B = bytes / HBM
+    bandwidth; the larger one binds.  Returns the roofline object in the binding unit plus the
+    fraction of the tensor peak and max(t_F, t_B) / t (the "% of roofline")."""
+    t = ms / 1e3
+    t_f = flops / (tensor_peak_tflops * 1e12)
+    t_b = nbytes / (hbm_peak_gbs * 1e9)
+    if t_b > t_f:
+        roof = {"bound": "hbm", "achieved": nbytes / t / 1e9, "peak": hbm_peak_gbs, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / t / 1e12, "peak": tensor_peak_tflops, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["tensor_frac"] = flops / t / 1e12 / tensor_peak_tflops
+    roof["roofline_frac"] = max(t_f, t_b) / t
+    return roof
 
 
 def decode_formats(dev, pk, steps=50):
@@ -744,9 +767,11 @@ def main():
         ratio = {"nvfp4": 6.0, "fp8": 2.0, "fp8_f32sf": 2.0, "bf16": 1.0}[args.fmt]
         fp8_peak = ratio * pk["bf16_tflops"]
         gflops = 2.0 * int(counts.sum()) * w.N * w.K
-        achieved = gflops / (first_gemm_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                "frac": achieved / fp8_peak, "peak_src": f"{ratio:g} x bf16 burst ({pk['src']})"}
+        # near the ridge point: the gate-up GEMM's binding roofline (flops / tensor peak against
+        # algorithmic bytes / HBM bandwidth)
+        roof = binding_roofline(gflops, bytes_by_kernel["gemm"], first_gemm_ms, fp8_peak, pk["hbm_gbs"])
+        roof["peak_src"] = (f"{ratio:g} x bf16 burst ({pk['src']})" if roof["bound"] == "tensor"
+                            else pk["src"]) + f"; tensor peak {fp8_peak:.0f} TFLOP/s = {ratio:g} x bf16 burst"
     else:
         value = job_throughput(step_bytes, args.steps, world, elapsed_ms, 1e9)
         achieved = bytes_by_kernel["gemm"] / (first_gemm_ms / 1e3) / 1e9

@@ -49,3 +49,13 @@ def test_two_gemm_step_counts_the_second_gemm():
     b, flops = bench.step_work(w, counts, int(counts.sum()), fmt="fp8")
     assert {"gemm", "gemm2", "quantise2"} <= set(b)
     assert flops == 2.0 * counts.sum() * (w.N * w.K + w.N2 * w.K2)
+
+
+def test_binding_roofline_picks_the_longer_bound():
+    # 1 TFLOP and 1 GB in 1 ms: t_F = 1e12 / 2e15 = 0.5 ms, t_B = 1e9 / 2e12 = 0.5 ms -> equal; nudge each way
+    r = bench.binding_roofline(1e12, 1.2e9, 1.0, 2000.0, 2000.0)
+    assert r["bound"] == "hbm" and abs(r["achieved"] - 1200.0) < 1e-9 and abs(r["frac"] - 0.6) < 1e-12
+    assert abs(r["tensor_frac"] - 0.5) < 1e-12 and abs(r["roofline_frac"] - 0.6) < 1e-12
+    r = bench.binding_roofline(1.6e12, 1.0e9, 1.0, 2000.0, 2000.0)
+    assert r["bound"] == "tensor" and abs(r["achieved"] - 1600.0) < 1e-9 and abs(r["frac"] - 0.8) < 1e-12
+    assert abs(r["roofline_frac"] - 0.8) < 1e-12
