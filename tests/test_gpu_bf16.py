@@ -132,3 +132,32 @@ def test_bf16_end_to_end(dev, name):
             check_expert_block(yg[s:s + c], y_ref[s:s + c], f"bf16 {name} expert {e}")
     rms = expert_row_rms(y_ref, r["seg_start"], r["counts"])
     check_combined(bits16(z), z_ref, y_ref, r["output_index"], p.numpy(), rms, f"bf16 {name} combined")
+
+
+def test_masked_many_experts(dev):
+    """More than 256 experts: the small-slot tile with 1024-expert tables."""
+    rng = np.random.default_rng(7)
+    E, N, K, max_m = 260, 128, 128, 32
+    masked = rng.integers(0, max_m + 1, E)
+    x, w = _operands(E * max_m, E, N, K, 70)
+    d = torch.full((E * max_m, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    ops.grouped_gemm_bf16_masked(x.to(dev), w.to(dev), torch.as_tensor(masked, dtype=torch.int32, device=dev),
+                                 max_m, d=d)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    _check(d, x, w, np.arange(E + 1) * max_m, masked, "bf16 masked E=260")
+
+
+def test_route_bf16_above_the_single_launch_limit(dev):
+    rng = np.random.default_rng(8)
+    T, kr, E, K = 2500, 8, 64, 256
+    ids = np.stack([rng.permutation(E)[:kr] for _ in range(T)]).astype(np.int32)
+    x, _ = _operands(T, 1, 128, K, 71)
+    bufs = ops.route(torch.from_numpy(ids).to(dev), E, ops.CONTIGUOUS, 128, q=x.to(dev), fmt="bf16")
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    r = oracle.route.route(ids, E, ops.CONTIGUOUS, align=128)
+    assert np.array_equal(i32(bufs.output_index), r["output_index"])
+    tok = r["token_of_row"]
+    rows = np.nonzero(tok >= 0)[0]
+    assert np.array_equal(bits16(bufs.a_packed)[rows], bits16(x)[tok[rows]])

@@ -154,3 +154,39 @@ def test_f32sf_end_to_end(dev, name):
             check_expert_block(yg[s:s + c], y_ref[s:s + c], f"f32sf {name} expert {e}")
     rms = expert_row_rms(y_ref, r["seg_start"], r["counts"])
     check_combined(bits16(z), z_ref, y_ref, r["output_index"], p.numpy(), rms, f"f32sf {name} combined")
+
+
+def test_weights_in_pinned_host_memory_match_device_weights(dev):
+    counts = np.array([5, 0, 70, 40])
+    E, N, K = len(counts), 256, 512
+    seg = np.concatenate([[0], np.cumsum(counts)])
+    x, w = _x(int(seg[-1]), K, 80), _w(E, N, K, 81)
+    aq, asf = ops.quantise_act_f32sf(x.to(dev))
+    bq, bsf = ops.quantise_weight_f32sf(w.to(dev))
+    segt = torch.as_tensor(seg, dtype=torch.int32, device=dev)
+    ct = torch.as_tensor(counts, dtype=torch.int32, device=dev)
+    d_dev = ops.grouped_gemm_f32sf_contig(aq, asf, bq, bsf, segt, ct)
+    d_host = ops.grouped_gemm_f32sf_contig(aq, asf, bq.cpu().pin_memory(), bsf.cpu().pin_memory(), segt, ct,
+                                           flags=ops.B_HOST_MAPPED)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    for e in range(E):
+        s, c = int(seg[e]), int(counts[e])
+        assert torch.equal(d_host[s:s + c].view(torch.int16), d_dev[s:s + c].view(torch.int16))
+
+
+def test_route_f32sf_above_the_single_launch_limit(dev):
+    rng = np.random.default_rng(9)
+    T, kr, E, K = 2500, 8, 64, 384
+    ids = np.stack([rng.permutation(E)[:kr] for _ in range(T)]).astype(np.int32)
+    x = _x(T, K, 82)
+    q, sf = ops.quantise_act_f32sf(x.to(dev))
+    bufs = ops.route(torch.from_numpy(ids).to(dev), E, ops.CONTIGUOUS, 1, q=q, sf=sf, fmt="fp8_f32sf")
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    r = oracle.route.route(ids, E, ops.CONTIGUOUS, align=1)
+    tok = r["token_of_row"]
+    rows = np.nonzero(tok >= 0)[0]
+    q_ref, s_ref = oracle.f32sf.quantise_act(bits16(x))
+    assert np.array_equal(u8(bufs.a_packed)[rows], q_ref[tok[rows]])
+    assert np.array_equal(bufs.sfa_packed.cpu().numpy()[:, rows], s_ref.T[:, tok[rows]])

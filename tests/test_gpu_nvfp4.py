@@ -254,3 +254,61 @@ def test_nvfp4_end_to_end(dev, name, fused):
             check_expert_block(yg[s:s + c], y_ref[s:s + c], f"nvfp4 {name} expert {e}")
     rms = expert_row_rms(y_ref, r["seg_start"], r["counts"])
     check_combined(bits16(z), z_ref, y_ref, r["output_index"], p.numpy(), rms, f"nvfp4 {name} combined")
+
+
+def test_weights_in_pinned_host_memory_match_device_weights(dev):
+    counts = np.array([5, 0, 130, 40])
+    E, N, K = len(counts), 256, 512
+    seg = np.concatenate([[0], np.cumsum(counts)])
+    ops_, _ = _gemm_operands(int(seg[-1]), E, N, K, 60, dev)
+    aq, asf, bq, sfb, b_exp = ops_
+    segt = torch.as_tensor(seg, dtype=torch.int32, device=dev)
+    ct = torch.as_tensor(counts, dtype=torch.int32, device=dev)
+    d_dev = ops.grouped_gemm_nvfp4_contig(aq, asf, 0, bq, sfb, b_exp, segt, ct)
+    d_host = ops.grouped_gemm_nvfp4_contig(aq, asf, 0, bq.cpu().pin_memory(), sfb.cpu().pin_memory(), b_exp, segt, ct,
+                                           flags=ops.B_HOST_MAPPED)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    for e in range(E):
+        s, c = int(seg[e]), int(counts[e])
+        assert torch.equal(d_host[s:s + c].view(torch.int16), d_dev[s:s + c].view(torch.int16))
+
+
+def test_route_nvfp4_above_the_single_launch_limit(dev):
+    """20000 assignments: the multi-block route path scatters the NVFP4 rows and scale words."""
+    rng = np.random.default_rng(12)
+    T, kr, E, K = 2500, 8, 64, 512
+    ids = np.stack([rng.permutation(E)[:kr] for _ in range(T)]).astype(np.int32)
+    x = _x(T, K, 13)
+    q, sf = ops.quantise_act_nvfp4(x.to(dev), 0)
+    bufs = ops.route(torch.from_numpy(ids).to(dev), E, ops.CONTIGUOUS, 128, q=q, sf=sf, fmt="nvfp4")
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    r = oracle.route.route(ids, E, ops.CONTIGUOUS, align=128)
+    assert np.array_equal(i32(bufs.output_index), r["output_index"])
+    tok = r["token_of_row"]
+    rows = np.nonzero(tok >= 0)[0]
+    q_ref, sf_ref, _ = oracle.nvfp4.quantise_act(bits16(x), 0)
+    assert np.array_equal(u8(bufs.a_packed)[rows], q_ref[tok[rows]])
+    assert np.array_equal(bufs.sfa_packed.cpu().numpy()[:, rows], sf_ref[:, tok[rows]])
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_dispatch_nvfp4_random_small_batches(dev, seed):
+    rng = np.random.default_rng(200 + seed)
+    T, kr = int(rng.integers(1, 1200)), int(rng.integers(1, 9))
+    E = int(rng.integers(1, 257))
+    K = int(rng.choice([64, 576, 1024]))
+    ids = rng.integers(-1, E, (T, kr)).astype(np.int32)
+    x = _x(T, K, 300 + seed)
+    for layout, a in ((ops.CONTIGUOUS, 1), (ops.MASKED, 32)):
+        got = ops.dispatch_nvfp4(x.to(dev), torch.from_numpy(ids).to(dev), E, layout, a, a_exp=2)
+        torch.cuda.synchronize()
+        r = oracle.route.route(ids, E, layout, align=a, max_m=a)
+        assert np.array_equal(i32(got.output_index), r["output_index"])
+        tok = r["token_of_row"]
+        rows = np.nonzero(tok >= 0)[0]
+        q_ref, sf_ref, _ = oracle.nvfp4.quantise_act(bits16(x), 2)
+        assert np.array_equal(u8(got.a_packed)[rows], q_ref[tok[rows]])
+        assert np.array_equal(got.sfa_packed.cpu().numpy()[:, rows], sf_ref[:, tok[rows]])
+        ops.device_error()          # masked overflow is expected for some batches; clear it
