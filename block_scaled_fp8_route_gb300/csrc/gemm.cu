@@ -103,7 +103,8 @@ struct Cfg {
   static constexpr int kStageSf = (kSfStageBytes + 127) / 128 * 128;
   static constexpr int kAccBufs = kF32 ? 4 : (CPS == 1 && TOK <= 224) ? 2 : 1;
   static constexpr int kSfSlots = (kBf16 || kF32) ? 1 : kFp4 ? 4 : (CPS == 1 && TOK <= 224) ? 4 : 2;
-  static constexpr int kTokSfCols = (TOK + 31) / 32;
+  static constexpr int kTokSfCols = (TOK + 31) / 32;           // token-SF TMEM columns per MMA
+  static_assert(kTokSfCols >= 1 && kTokSfCols <= 14, "token SF columns");
   static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK <= 128 ? 64 : TOK <= 224 ? 56 : 224;   // token rows per TMA box
   // Launched as a programmatic dependent of the preceding kernel (dispatch / route / quantise)
   // only for the small-batch tile: there the launch and prologue overlap that kernel's tail
