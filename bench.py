@@ -11,6 +11,8 @@ path) on a bounded sample of the same workload, on the host cores.
 """
 
 import argparse
+import collections
+import contextlib
 import hashlib
 import json
 import os
@@ -707,29 +709,27 @@ def main():
     for _ in range(args.warmup):
         path.step(x, ids, p, h2)
 
-    # eager steps, with CUDA events around every GEMM launch on the launching stream
-    gemm_events = []
-    orig_gemm = path.gemm
+    # eager steps, with CUDA events around every stage (dispatch / quantise / route, GEMMs, combine)
+    # on the launching stream
+    stage_events = collections.defaultdict(list)
 
-    def timed_gemm(*a, **k):
+    @contextlib.contextmanager
+    def stage_timer(name):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        r = orig_gemm(*a, **k)
+        yield
         e1.record(stream)
-        gemm_events.append((e0, e1))
-        return r
+        stage_events[name].append((e0, e1))
 
-    path.gemm = timed_gemm
     torch.cuda.synchronize()
     q0 = torch.cuda.Event(enable_timing=True)
     q1 = torch.cuda.Event(enable_timing=True)
     q0.record(stream)
     for _ in range(args.steps):
-        path.step(x, ids, p, h2)
+        path.step(x, ids, p, h2, timer=stage_timer)
     q1.record(stream)
     torch.cuda.synchronize()
-    path.gemm = orig_gemm
     eager_ms = q0.elapsed_time(q1) / args.steps
 
     # the timed region: the same step replayed from a CUDA graph (launch gaps removed)
@@ -754,10 +754,12 @@ def main():
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), dev)
     assert ops.device_error() == 0, "device error during the timed steps"
 
-    gemm_ms = [a.elapsed_time(b) for a, b in gemm_events]
-    n_gemm_per_step = 2 if w.K2 else 1
+    stage_ms = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in stage_events.items()}
     # dominant kernel: the first (gate-up) GEMM
-    first_gemm_ms = statistics.mean(gemm_ms[0::n_gemm_per_step])
+    first_gemm_ms = stage_ms["gemm"]
+    per_kernel = {k: {"bytes": bytes_by_kernel[k], "us": stage_ms[k] * 1e3,
+                      "gbs": bytes_by_kernel[k] / (stage_ms[k] / 1e3) / 1e9}
+                  for k in stage_ms if k in bytes_by_kernel}
     launches_per_step = path.launches_per_step()
 
     if large_m:
@@ -860,7 +862,7 @@ def main():
             "step_bytes": step_bytes, "step_gemm_flops": flops, "eager_ms_per_step": eager_ms,
             "timed": "CUDA-graph replays of the whole step (eager step time in eager_ms_per_step)",
             "large_m_gemm": large_m if large_m is not None else None,
-            "per_kernel_bytes": bytes_by_kernel,
+            "per_kernel": per_kernel,
             "hbm_stream_read_gbs": hbm_read,
             "decode_formats": formats,
         }

@@ -12,9 +12,16 @@ construction (``quantise_weight`` + ``prepare_weight_sf``, or
 one stream.
 """
 
+import contextlib
+
 import torch
 
 from . import ops
+
+
+@contextlib.contextmanager
+def _no_timer(name):
+    yield
 
 
 class MoEPath:
@@ -119,32 +126,50 @@ class MoEPath:
                                            expected_m=self.expected_m, flags=self.flags)
         return ops.grouped_gemm_contig(a, sfa, wq, sfb, b.seg_start, b.counts, d=d, flags=self.flags)
 
-    def step(self, x, topk_ids, topk_weights, h2=None, z=None):
+    def step(self, x, topk_ids, topk_weights, h2=None, z=None, timer=None):
         """Run the whole path; ``h2`` is the packed bf16 [m_cap, K2] input of the second GEMM;
         the combined output goes to ``z`` (default: this object's output buffer).  Small batches
-        quantise, route and scatter in one launch (``dispatch``)."""
-        if self.fused_dispatch and self.fmt == "nvfp4":
-            ops.dispatch_nvfp4(x, topk_ids, self.E, self.layout, self.align_or_max_m, a_exp=self.a_exp,
-                               bufs=self.bufs)
-        elif self.fused_dispatch:
-            ops.dispatch(x, topk_ids, self.E, self.layout, self.align_or_max_m, bufs=self.bufs)
-        elif self.fmt == "bf16":
-            ops.route(topk_ids, self.E, self.layout, self.align_or_max_m, q=x, bufs=self.bufs, fmt="bf16")
-        else:
-            self._quantise(x, self.q, self.sf)
-            ops.route(topk_ids, self.E, self.layout, self.align_or_max_m, q=self.q, sf=self.sf, bufs=self.bufs,
-                      fmt=self.fmt)
-        self.gemm(self.bufs.a_packed, self.bufs.sfa_packed, self.wq, self.sfb, self.y, self.b_exp)
+        quantise, route and scatter in one launch (``dispatch``).  ``timer(name)``, if given, is a
+        context manager wrapped around each stage (``dispatch`` or ``quantise`` + ``route``,
+        ``gemm``, ``quantise2`` + ``gemm2``, ``combine``), e.g. to record CUDA events."""
+        t = timer if timer is not None else _no_timer
+        self._stage_in(x, topk_ids, t)
+        with t("gemm"):
+            self.gemm(self.bufs.a_packed, self.bufs.sfa_packed, self.wq, self.sfb, self.y, self.b_exp)
         out = self.y
         if self.two_gemms and self.fmt == "bf16":
-            self.gemm(h2, None, self.w2q, None, self.y2)
+            with t("gemm2"):
+                self.gemm(h2, None, self.w2q, None, self.y2)
+            out = self.y2
         elif self.two_gemms:
-            self._quantise(h2, self.q2, self.sf2)
-            self.gemm(self.q2, self.sf2, self.w2q, self.sfb2, self.y2, self.b2_exp)
+            with t("quantise2"):
+                self._quantise(h2, self.q2, self.sf2)
+            with t("gemm2"):
+                self.gemm(self.q2, self.sf2, self.w2q, self.sfb2, self.y2, self.b2_exp)
             out = self.y2
         z = self.z if z is None else z
-        ops.combine(out, self.bufs.output_index, topk_weights, z=z)
+        with t("combine"):
+            ops.combine(out, self.bufs.output_index, topk_weights, z=z)
         return z
+
+    def _stage_in(self, x, topk_ids, t):
+        """Quantise + route + scatter of the activations into the packed operand."""
+        if self.fused_dispatch and self.fmt == "nvfp4":
+            with t("dispatch"):
+                ops.dispatch_nvfp4(x, topk_ids, self.E, self.layout, self.align_or_max_m, a_exp=self.a_exp,
+                                   bufs=self.bufs)
+        elif self.fused_dispatch:
+            with t("dispatch"):
+                ops.dispatch(x, topk_ids, self.E, self.layout, self.align_or_max_m, bufs=self.bufs)
+        elif self.fmt == "bf16":
+            with t("route"):
+                ops.route(topk_ids, self.E, self.layout, self.align_or_max_m, q=x, bufs=self.bufs, fmt="bf16")
+        else:
+            with t("quantise"):
+                self._quantise(x, self.q, self.sf)
+            with t("route"):
+                ops.route(topk_ids, self.E, self.layout, self.align_or_max_m, q=self.q, sf=self.sf, bufs=self.bufs,
+                          fmt=self.fmt)
 
     def capture(self, x, topk_ids, topk_weights, h2=None):
         """Record one step on these (static) input tensors into a CUDA graph.
