@@ -16,7 +16,9 @@ namespace {
 
 constexpr int kMaxKr = 32;
 
-__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y, int64_t y_rows,
+// At most 64 registers (four CTAs per SM): with 66 the kernel held three and large batches ran
+// 11-12 % slower (bandwidth-bound, occupancy-limited; same-box A/B, bit-identical output).
+__global__ void __launch_bounds__(256, 4) combine_kernel(const uint16_t* __restrict__ y, int64_t y_rows,
                                                       const int32_t* __restrict__ output_index,
                                                       const float* __restrict__ topk_weights, int64_t T, int kr,
                                                       int64_t N, uint16_t* __restrict__ z) {
