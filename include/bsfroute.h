@@ -3,7 +3,12 @@
  *
  * C ABI of the hot path:
  *   quantise_act  -> route (+ scatter) -> grouped_gemm_{contig,masked} -> combine
- * plus the once-per-weight-load steps quantise_weight and prepare_weight_sf.
+ * plus the once-per-weight-load steps quantise_weight and prepare_weight_sf,
+ * and for small batches dispatch (quantise + route + scatter in one launch).
+ * The same path on the pages' other operand formats, declared further down:
+ *   NVFP4  (E2M1 + one UE4M3 scale per 16 values, *_nvfp4),
+ *   BF16   (unquantised, *_bf16),
+ *   FP8 with float32 scale factors (*_f32sf).
  *
  * Conventions of every entry point
  *   - Pointers are DEVICE pointers (CUDA global memory) unless a parameter says
