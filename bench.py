@@ -498,6 +498,39 @@ def run_host_sweep(args, w, metric):
                       "link_gbs": link_bytes / (gemm_ms / 1e3) / 1e9, "tflops": flops / (gemm_ms / 1e3) / 1e12})
     clk = clocks.stop()
     last = sweep[-1]
+    # end to end at the last T: pinned host batches in, output back, every step (HostStreamedPath)
+    from block_scaled_fp8_route_gb300 import HostStreamedPath
+    wl = W.with_tokens(w, last["T"])
+    x_h = W.activations(wl).pin_memory()
+    ids_h, p_h = (t.pin_memory() for t in W.routing(wl))
+    streamed = HostStreamedPath(path, wl.T, wl.K, wl.kr, device=dev)
+    outs = [torch.empty(path.z.shape, dtype=path.z.dtype).pin_memory() for _ in range(4)]
+    batches = [(x_h, ids_h, p_h)] * args.steps
+    streamed.run(batches[:2], outs[:2])
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    streamed.run(batches, [outs[i % 4] for i in range(args.steps)], start_event=s0, end_event=s1)
+    torch.cuda.synchronize()
+    e2e_ms = s0.elapsed_time(s1) / args.steps
+    link_bytes_last = last["link_gbs"] * last["gemm_ms"] / 1e3 * 1e9
+    e2e = {"value": link_bytes_last / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (x_h, ids_h, p_h)),
+           "d2h_bytes_per_step": outs[0].numel() * outs[0].element_size(), "ms_per_step": e2e_ms,
+           "how": "pinned host batches -> device -> whole path (graph, weights read from host memory) -> "
+                  "pinned host output, every step (HostStreamedPath)"}
+    del streamed
+    # the oracle on a bounded sample of the same T (the busiest two experts), on the host cores
+    cpu = None
+    if not args.no_cpu_baseline:
+        sample = OracleSample(wl, 2)
+        tot_t = tot_b = 0.0
+        reps = 0
+        while tot_t < 10.0 and reps < 50:
+            dt, b, _ = sample.run()
+            tot_t, tot_b, reps = tot_t + dt, tot_b + b, reps + 1
+        cpu = {"value": tot_b / tot_t / 1e9, "unit": "GB/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"{sample.desc}; T={wl.T}; {reps} passes; bytes = weights and rows of the sampled experts",
+               "seconds": tot_t}
     line = {
         "metric": metric, "value": last["link_gbs"], "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": last["step_ms"], "higher_is_better": True, "scaling": "weak",
@@ -508,7 +541,7 @@ def run_host_sweep(args, w, metric):
                      "frac": last["link_gbs"] / link_gbs, "peak_src": "measured SM stream read of 1 GiB pinned host memory",
                      "traffic": None, "kernel": "grouped_gemm_kernel"},
         "host_link": {"sm_read_gbs": link_gbs, "memcpy_h2d_gbs": memcpy_gbs},
-        "sweep": sweep, "clocks": clk, "cpu_baseline": None, "e2e": None,
+        "sweep": sweep, "clocks": clk, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": path.launches_per_step() * args.steps,
     }
     print(json.dumps(line), flush=True)
