@@ -568,15 +568,16 @@ def large_m_gemms(dev, pk, reps=10):
             wt = W.weights(w, device=dev, N=N, K=K, tag=tag)
             bq, sf128 = ops.quantise_weight(wt)
             del wt
+            bq = ops.tile_weights(bq)           # the layout MoEPath uses
             sfb = ops.prepare_weight_sf(sf128, K)
             d = torch.empty((bufs.m_cap, N), dtype=torch.bfloat16, device=dev)
             for _ in range(3):
-                ops.grouped_gemm_contig(aq, asf, bq, sfb, bufs.seg_start, bufs.counts, d=d)
+                ops.grouped_gemm_contig(aq, asf, bq, sfb, bufs.seg_start, bufs.counts, d=d, flags=ops.B_TILED)
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
             e0.record()
             for _ in range(reps):
-                ops.grouped_gemm_contig(aq, asf, bq, sfb, bufs.seg_start, bufs.counts, d=d)
+                ops.grouped_gemm_contig(aq, asf, bq, sfb, bufs.seg_start, bufs.counts, d=d, flags=ops.B_TILED)
             e1.record()
             torch.cuda.synchronize()
             ms = e0.elapsed_time(e1) / reps

@@ -34,6 +34,7 @@ SIGNATURES = {
     "bsf_grouped_gemm_masked": (_c_int, [_p, _p, _i64, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _c_int, _p]),
     "bsf_combine": (_c_int, [_p, _i64, _p, _p, _i64, _i64, _i64, _p, _p]),
     "bsf_checksum_u64": (_c_int, [_p, _size, _c_int, _p, _p]),
+    "bsf_tile_weights": (_c_int, [_p, _i64, _i64, _i64, _p, _p]),
     "bsf_route_nvfp4": (_c_int, [_p, _i64, _i64, _i64, _c_int, _i64, _p, _p, _p, _p, _p, _i64,
                                  _p, _p, _i64, _i64, _p, _p, _i64, _p, _size, _p]),
     "bsf_route_bf16": (_c_int, [_p, _i64, _i64, _i64, _c_int, _i64, _p, _p, _p, _p, _p, _i64, _p, _i64, _p, _p,

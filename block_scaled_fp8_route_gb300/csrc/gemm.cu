@@ -57,7 +57,7 @@ struct GemmArgs {
   uint16_t* d;
   int E, N, K;
   int* err;
-  int withhold_loads;        // test-only fault injection (BSF_DEBUG_WITHHOLD_LOADS)
+  int flags;                 // BSF_B_TILED (weight layout), BSF_DEBUG_WITHHOLD_LOADS (test-only fault injection)
   int a_exp;                 // NVFP4: tensor exponent of A
   const int32_t* b_exp;      // NVFP4: tensor exponent per expert of B [E]
   const float* sfa_f32;      // FP32 scales: A [K/128][sfa_ld]
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       int issued = 0;
-      bool ok = !p.withhold_loads;
+      bool ok = !(p.flags & BSF_DEBUG_WITHHOLD_LOADS);
       for (int t = t_first; t < total_tiles && ok; t += G) {
         const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
         const int n_loads = (tl.ntok + C::kBoxRows - 1) / C::kBoxRows;
@@ -321,7 +321,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(stage_b + stage * C::kStageB, &tmap_b, &full[stage], kb * kBlockK, wrow);
+          if (p.flags & BSF_B_TILED)   // weights pre-tiled: box (e, nt, kb) is 16 KB contiguous
+            tma_load_2d(stage_b + stage * C::kStageB, &tmap_b, &full[stage], 0,
+                        ((tl.e * nnt + tl.nt) * nkb + kb) * kBlockW);
+          else
+            tma_load_2d(stage_b + stage * C::kStageB, &tmap_b, &full[stage], kb * kBlockK, wrow);
           for (int i = 0; i < n_loads; ++i)
             tma_load_2d(stage_a + stage * C::kStageA + i * C::kBoxRows * kBlockK, &tmap_a, &full[stage],
                         kb * kBlockK, tl.tok0 + i * C::kBoxRows);
@@ -717,7 +721,13 @@ bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int6
   CUtensorMap map_a, map_b;
   const int64_t row_bytes = C::kFp4 ? args.K / 2 : C::kBf16 ? 2 * args.K : args.K;
   if (!make_map(&map_a, a, args.m_rows, row_bytes, C::kBoxRows)) return BSF_ERR_CUDA;
-  if (!make_map(&map_b, b, static_cast<int64_t>(args.E) * args.N, row_bytes, kBlockW)) return BSF_ERR_CUDA;
+  if (args.flags & BSF_B_TILED) {   // [E][N/128][row_bytes/128] boxes of 128 rows x 128 bytes, each contiguous
+    if (static_cast<int64_t>(args.E) * args.N * (row_bytes / 128) > INT32_MAX) return BSF_ERR_UNSUPPORTED;
+    if (!make_map(&map_b, b, static_cast<int64_t>(args.E) * args.N * (row_bytes / 128), 128, kBlockW))
+      return BSF_ERR_CUDA;
+  } else if (!make_map(&map_b, b, static_cast<int64_t>(args.E) * args.N, row_bytes, kBlockW)) {
+    return BSF_ERR_CUDA;
+  }
   CUtensorMap map_sfb = map_b, map_sfa = map_a;     // placeholders: only NVFP4 stages load scale words by TMA
   if (C::kFp4) {
     const int64_t nw = args.K / 64;
@@ -774,7 +784,7 @@ bsf_status check_common(const uint8_t* a, const int32_t* sfa, int64_t sfa_ld, in
   if (E <= 0 || E > kMaxExperts || N <= 0 || K <= 0 || N % 128 || K % 128) return BSF_ERR_INVALID_ARGUMENT;
   if (nvfp4 && K % 256) return BSF_ERR_INVALID_ARGUMENT;
   if (nvfp4 && E > kNvfp4MaxE) return BSF_ERR_UNSUPPORTED;
-  if (flags & ~(BSF_B_HOST_MAPPED | BSF_DEBUG_WITHHOLD_LOADS)) return BSF_ERR_INVALID_ARGUMENT;
+  if (flags & ~(BSF_B_HOST_MAPPED | BSF_B_TILED | BSF_DEBUG_WITHHOLD_LOADS)) return BSF_ERR_INVALID_ARGUMENT;
   if (!a || !sfa || !b || !sfb || !d) return BSF_ERR_INVALID_ARGUMENT;
   if (sfa_ld < m_rows || sfa_ld % 4) return BSF_ERR_INVALID_ARGUMENT;
   if (!aligned16(a) || !aligned16(b) || !aligned16(d) || !aligned16(sfa) || !aligned16(sfb))
@@ -801,7 +811,7 @@ extern "C" bsf_status bsf_grouped_gemm_contig(const uint8_t* a, const int32_t* s
   if (!err) return BSF_ERR_CUDA;
   GemmArgs args{seg_start, counts, 0, m_cap, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
                 static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
-                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0};
+                flags};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (flags & BSF_B_HOST_MAPPED) {   // one tile per (expert, N-tile) up to 448 rows: weights cross the link once
     const int64_t max_tiles = (m_cap / kHostTok + E) * (N / 128);
@@ -825,7 +835,7 @@ extern "C" bsf_status bsf_grouped_gemm_masked(const uint8_t* a, const int32_t* s
   if (!err) return BSF_ERR_CUDA;
   GemmArgs args{nullptr, masked_m, max_m, m_rows, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
                 static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
-                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0};
+                flags};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t hint = expected_m > 0 ? expected_m : max_m;
   const bool host = (flags & BSF_B_HOST_MAPPED) != 0;
@@ -863,7 +873,7 @@ extern "C" bsf_status bsf_grouped_gemm_nvfp4_contig(const uint8_t* a, const int3
   if (!err) return BSF_ERR_CUDA;
   GemmArgs args{seg_start, counts, 0, m_cap, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
                 static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
-                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0, a_exp, b_exp};
+                flags, a_exp, b_exp};
   const int64_t max_tiles = (m_cap / 128 + E) * (N / 128);
   return launch<128, 2, kNvfp4MaxE, kFmtNvfp4>(args, a, b, max_tiles, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -884,7 +894,7 @@ extern "C" bsf_status bsf_grouped_gemm_nvfp4_masked(const uint8_t* a, const int3
   if (!err) return BSF_ERR_CUDA;
   GemmArgs args{nullptr, masked_m, max_m, m_rows, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
                 static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
-                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0, a_exp, b_exp};
+                flags, a_exp, b_exp};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t hint = expected_m > 0 ? expected_m : max_m;
   if (max_m <= 64 || ((flags & BSF_B_HOST_MAPPED) == 0 && hint <= 32)) {
@@ -905,7 +915,7 @@ namespace {
 bsf_status check_bf16(const void* a, int64_t m_rows, const void* b, const void* d, int64_t E, int64_t N, int64_t K,
                       int flags, const uint8_t** b_dev) {
   if (E <= 0 || E > kMaxExperts || N <= 0 || K <= 0 || N % 128 || K % 64) return BSF_ERR_INVALID_ARGUMENT;
-  if (flags & ~(BSF_B_HOST_MAPPED | BSF_DEBUG_WITHHOLD_LOADS)) return BSF_ERR_INVALID_ARGUMENT;
+  if (flags & ~(BSF_B_HOST_MAPPED | BSF_B_TILED | BSF_DEBUG_WITHHOLD_LOADS)) return BSF_ERR_INVALID_ARGUMENT;
   if (!a || !b || !d) return BSF_ERR_INVALID_ARGUMENT;
   if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return BSF_ERR_MISALIGNED;
   if (m_rows > INT32_MAX || E * N > INT32_MAX || K > (1 << 23)) return BSF_ERR_UNSUPPORTED;
@@ -936,7 +946,7 @@ extern "C" bsf_status bsf_grouped_gemm_bf16_contig(const void* a, int64_t m_cap,
   if (!err) return BSF_ERR_CUDA;
   GemmArgs args{seg_start, counts, 0, m_cap, nullptr, 0, nullptr, static_cast<uint16_t*>(d),
                 static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
-                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0};
+                flags};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint8_t* ad = static_cast<const uint8_t*>(a);
   if (flags & BSF_B_HOST_MAPPED) {
@@ -960,7 +970,7 @@ extern "C" bsf_status bsf_grouped_gemm_bf16_masked(const void* a, const void* b,
   if (!err) return BSF_ERR_CUDA;
   GemmArgs args{nullptr, masked_m, max_m, m_rows, nullptr, 0, nullptr, static_cast<uint16_t*>(d),
                 static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
-                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0};
+                flags};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint8_t* ad = static_cast<const uint8_t*>(a);
   const int64_t hint = expected_m > 0 ? expected_m : max_m;
@@ -1000,7 +1010,7 @@ extern "C" bsf_status bsf_grouped_gemm_f32sf_contig(const uint8_t* a, const floa
   if (!err) return BSF_ERR_CUDA;
   GemmArgs args{seg_start, counts, 0, m_cap, nullptr, sfa_ld, nullptr, static_cast<uint16_t*>(d),
                 static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
-                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0, 0, nullptr, sfa, reinterpret_cast<const float*>(sfb_i)};
+                flags, 0, nullptr, sfa, reinterpret_cast<const float*>(sfb_i)};
   const int64_t max_tiles = (m_cap / 64 + E) * (N / 128);
   return launch<64, 1, kMaxExperts, kFmtFp8F32>(args, a, b, max_tiles, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1021,7 +1031,7 @@ extern "C" bsf_status bsf_grouped_gemm_f32sf_masked(const uint8_t* a, const floa
   if (!err) return BSF_ERR_CUDA;
   GemmArgs args{nullptr, masked_m, max_m, m_rows, nullptr, sfa_ld, nullptr, static_cast<uint16_t*>(d),
                 static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
-                (flags & BSF_DEBUG_WITHHOLD_LOADS) != 0, 0, nullptr, sfa, reinterpret_cast<const float*>(sfb_i)};
+                flags, 0, nullptr, sfa, reinterpret_cast<const float*>(sfb_i)};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // small slots or small typical counts: 32-token tiles, two CTAs per SM (32 accumulators per thread);
   // same-box A/B at decode: 258 us against 329 us for the 64-token tile with one CTA per SM

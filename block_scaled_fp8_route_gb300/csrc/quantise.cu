@@ -1,5 +1,5 @@
-// Quantisers: bf16 -> FP8 E4M3 with power-of-two (UE8M0) block scales, and the
-// weight scale-factor transform.
+// Quantisers: bf16 -> FP8 E4M3 with power-of-two (UE8M0) block scales, the
+// weight scale-factor transform, and the tiled weight layout.
 //
 // DeepGEMM FP8 article (nxmr.cn), "补偿机制一": every scale is an exact power
 // of two, packed as UE8M0 bytes four to an int32; "补偿机制三": SFs are
@@ -147,10 +147,39 @@ __global__ void prepare_weight_sf_kernel(const float* __restrict__ sf128, int64_
   sfb[idx] = static_cast<int32_t>(word);
 }
 
+// Weight tiling: one thread per 16 output bytes.  Output block (e, nt, kb) is
+// the 128 x 128-byte piece of expert e at rows 128 nt.., bytes 128 kb.., its
+// rows 128 bytes apart; eight consecutive threads read one 128-byte row piece.
+__global__ void __launch_bounds__(256) tile_weights_kernel(const uint4* __restrict__ b, int64_t N, int64_t row_bytes,
+                                                           int64_t n16, uint4* __restrict__ out) {
+  const int64_t nkb = row_bytes / 128, nnt = N / 128, row16 = row_bytes / 16;
+  for (int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; o < n16;
+       o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t blk = o / 1024, r = (o / 8) % 128, c16 = o % 8;
+    const int64_t kb = blk % nkb, nt = (blk / nkb) % nnt, e = blk / (nkb * nnt);
+    out[o] = __ldg(b + (e * N + nt * 128 + r) * row16 + kb * 8 + c16);
+  }
+}
+
 }  // namespace
 }  // namespace bsf
 
 using namespace bsf;
+
+extern "C" bsf_status bsf_tile_weights(const uint8_t* b, int64_t E, int64_t N, int64_t row_bytes, uint8_t* out,
+                                       bsf_stream_t stream) {
+  if (E <= 0 || N <= 0 || row_bytes <= 0 || N % 128 || row_bytes % 128) return BSF_ERR_INVALID_ARGUMENT;
+  if (!b || !out || b == out) return BSF_ERR_INVALID_ARGUMENT;
+  if (!aligned16(b) || !aligned16(out)) return BSF_ERR_MISALIGNED;
+  if (E * N > INT32_MAX || E * N * (row_bytes / 128) > INT32_MAX) return BSF_ERR_UNSUPPORTED;
+  const int64_t n16 = E * N * row_bytes / 16;
+  int64_t blocks = static_cast<int64_t>(sm_count()) * 8;
+  const int64_t need = (n16 + 255) / 256;
+  if (need < blocks) blocks = need;
+  tile_weights_kernel<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(b), N, row_bytes, n16, reinterpret_cast<uint4*>(out));
+  return launch_status();
+}
 
 extern "C" bsf_status bsf_quantise_act(const void* x, int64_t T, int64_t K, uint8_t* q, int32_t* sf, int64_t sf_ld,
                                        bsf_stream_t stream) {

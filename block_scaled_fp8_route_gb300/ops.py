@@ -15,6 +15,7 @@ from . import _lib
 CONTIGUOUS = 0
 MASKED = 1
 B_HOST_MAPPED = 1
+B_TILED = 2              # weights in the layout of tile_weights()
 # device error bits (BSF_DEVERR_* in bsfroute.h), read with device_error()
 DEVERR_EXPERT_ID = 0x1
 DEVERR_MASKED_OVERFLOW = 0x2
@@ -79,6 +80,18 @@ def prepare_weight_sf(sf128, K: int, stream=None):
     _lib.check(_lib.load().bsf_prepare_weight_sf(_ptr(sf128.contiguous()), E, N, K, _ptr(sfb), _stream(stream)),
                "prepare_weight_sf")
     return sfb
+
+
+def tile_weights(b, stream=None):
+    """Weights [E, N, ...] (any dtype; rows of ``row_bytes`` bytes) -> the same bytes tiled
+    [E][N/128][row_bytes/128][128][128] for the GEMM flag ``B_TILED``; returned as uint8
+    [E, N, row_bytes] so that its shape still names the expert and row counts."""
+    E, N = b.shape[0], b.shape[1]
+    src = b.contiguous().view(torch.uint8).reshape(E, N, -1)
+    out = torch.empty_like(src)
+    _lib.check(_lib.load().bsf_tile_weights(_ptr(src), E, N, src.shape[2], _ptr(out), _stream(stream)),
+               "tile_weights")
+    return out
 
 
 def route_capacity(T: int, kr: int, E: int, layout: int, align_or_max_m: int) -> int:

@@ -31,12 +31,13 @@ class MoEPath:
     scales, applied per 128-K block in software)."""
 
     def __init__(self, E, kr, T, K, N, w_bf16, layout=ops.CONTIGUOUS, align_or_max_m=1, w2_bf16=None,
-                 device="cuda", weights_on_host=False, expected_m=0, fused_dispatch=None, fmt="fp8", a_exp=0):
+                 device="cuda", weights_on_host=False, expected_m=0, fused_dispatch=None, fmt="fp8", a_exp=0,
+                 tiled_weights=True):
         self.E, self.kr, self.T, self.K, self.N = E, kr, T, K, N
         self.layout, self.align_or_max_m = layout, align_or_max_m
         self.expected_m = expected_m
         self.fmt, self.a_exp = fmt, a_exp
-        self.flags = ops.B_HOST_MAPPED if weights_on_host else 0
+        self.flags = (ops.B_HOST_MAPPED if weights_on_host else 0) | (ops.B_TILED if tiled_weights else 0)
         self.wq, self.sfb, self.b_exp = self._weights(w_bf16.to(device), K)
         if weights_on_host:
             self.wq = self.wq.cpu().pin_memory()
@@ -60,6 +61,12 @@ class MoEPath:
             self.z = torch.empty((T, N), dtype=torch.bfloat16, device=device)
 
     def _weights(self, w, K):
+        wq, sfb, b_exp = self._quantised_weights(w, K)
+        if self.flags & ops.B_TILED:
+            wq = ops.tile_weights(wq)
+        return wq, sfb, b_exp
+
+    def _quantised_weights(self, w, K):
         if self.fmt == "bf16":
             return w.contiguous(), None, None
         if self.fmt == "fp8_f32sf":

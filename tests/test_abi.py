@@ -57,6 +57,12 @@ def test_argument_validation_needs_no_device(lib):
     assert lib.bsf_grouped_gemm_bf16_contig(nul, 8, nul, nul, nul, nul, 2, 128, 96, 0, nul) == 1
     # FP32 scales: N must be a multiple of 128
     assert lib.bsf_grouped_gemm_f32sf_masked(nul, nul, 8, nul, nul, nul, nul, 2, 4, 100, 128, 0, 0, nul) == 1
+    # weight tiling: rows of a multiple of 128 bytes, N a multiple of 128, distinct buffers
+    assert lib.bsf_tile_weights(nul, 2, 128, 96, nul, nul) == 1
+    assert lib.bsf_tile_weights(nul, 2, 100, 128, nul, nul) == 1
+    assert lib.bsf_tile_weights(nul, 2, 128, 128, nul, nul) == 1
+    # an undefined GEMM flag bit
+    assert lib.bsf_grouped_gemm_contig(nul, nul, 4, 4, nul, nul, nul, nul, nul, 2, 128, 128, 0x4, nul) == 1
 
 
 def test_python_constants_match_header():
@@ -71,5 +77,6 @@ def test_python_constants_match_header():
                  "DEVERR_SEGMENT"):
         assert getattr(ops, name) == defs[name], name
     assert ops.B_HOST_MAPPED == defs["B_HOST_MAPPED"]
+    assert ops.B_TILED == defs["B_TILED"]
     assert ops.DISPATCH_MAX_ASSIGNMENTS == defs["DISPATCH_MAX_ASSIGNMENTS"]
     assert ops.DISPATCH_MAX_EXPERTS == defs["DISPATCH_MAX_EXPERTS"]
