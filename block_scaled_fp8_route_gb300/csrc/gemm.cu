@@ -37,7 +37,6 @@ namespace {
 constexpr int kBlockW = 128;        // weight rows per tile (MMA M)
 constexpr int kBlockK = 128;        // K per pipeline stage (one 128-byte swizzle row of FP8)
 constexpr int kMaxExperts = 1024;
-constexpr int kThreads = 320;
 constexpr int kBigTok = 224;        // token tile of the large-segment variant
 constexpr int kHostTok = 448;       // token tile of the host-weight (K-outer / M-inner) variant
 constexpr int kFmtFp8 = 0;          // E4M3 operands, UE8M0 scales per 128 K (kind::mxf8f6f4, 1X)
@@ -82,7 +81,13 @@ struct GemmArgs {
 // scale words cover four stages (one byte per stage, picked by sf_id);
 // NVFP4 needs a word per row per MMA, so its SF slot covers one stage:
 // 4 x 4 weight columns + 4 x 4 token columns (tokens <= 128).
-template <int TOK, int CPS = 1, int MAXE = kMaxExperts, int FMT = kFmtFp8>
+// WT = weight tiles per work item.  WT = 2 (FP8, 224 tokens, one CTA per SM): a stage holds two
+// 128-row weight tiles and one token tile, and each K-step issues one MMA per weight tile into its
+// own 224-column accumulator, so a work item is a 256 x 224 output block.  The bytes a stage brings
+// into shared memory then cover 1.47x the MMA work of the 128 x 224 tile ((256 + 224) bytes per
+// 256 x 224 products against (128 + 224) per 128 x 224), which is what a latency-bound load
+// pipeline needs; the price is that the epilogue of one item no longer overlaps the next item's MMAs.
+template <int TOK, int CPS = 1, int MAXE = kMaxExperts, int FMT = kFmtFp8, int WT = 1>
 struct Cfg {
   static constexpr bool kFp4 = FMT == kFmtNvfp4;
   static constexpr bool kBf16 = FMT == kFmtBf16;            // no scale factors: SF warps idle
@@ -93,7 +98,7 @@ struct Cfg {
   static constexpr int kKElems = kFp4 ? 256 : kBf16 ? 64 : 128;   // K values per stage
   static constexpr int kKbPerSlot = kFp4 ? 1 : 4;            // stages per SF slot
   // NVFP4 stages also carry the stage's scale words (TMA), which costs one stage of ring depth
-  static constexpr int kStages = kFp4 ? (TOK <= 64 ? 3 : 2)
+  static constexpr int kStages = WT == 2 ? 3 : kFp4 ? (TOK <= 64 ? 3 : 2)
                                       : CPS == 2 ? (TOK <= 64 ? (MAXE <= 256 ? 4 : 3) : TOK <= 128 ? 3 : 2)
                                                  : TOK <= 64 ? 8 : TOK <= 224 ? 4 : 2;
   // NVFP4 scale words of one stage in shared memory: weights [4 MMAs][128 rows] int32 (box 128 x 4),
@@ -101,8 +106,8 @@ struct Cfg {
   static constexpr int kSfTokCols = TOK + 4;
   static constexpr int kSfStageBytes = kFp4 ? 4 * kBlockW * 4 + 4 * kSfTokCols * 4 : 0;
   static constexpr int kStageSf = (kSfStageBytes + 127) / 128 * 128;
-  static constexpr int kAccBufs = kF32 ? 4 : (CPS == 1 && TOK <= 224) ? 2 : 1;
-  static constexpr int kSfSlots = (kBf16 || kF32) ? 1 : kFp4 ? 4 : (CPS == 1 && TOK <= 224) ? 4 : 2;
+  static constexpr int kAccBufs = kF32 ? 4 : (CPS == 1 && TOK <= 224 && WT == 1) ? 2 : 1;
+  static constexpr int kSfSlots = (kBf16 || kF32) ? 1 : kFp4 ? 4 : (CPS == 1 && TOK <= 224 && WT == 1) ? 4 : 2;
   static constexpr int kTokSfCols = (TOK + 31) / 32;           // token-SF TMEM columns per MMA
   static_assert(kTokSfCols >= 1 && kTokSfCols <= 14, "token SF columns");
   static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK <= 128 ? 64 : TOK <= 224 ? 56 : 224;   // token rows per TMA box
@@ -115,18 +120,29 @@ struct Cfg {
   // memory); run only as many CTAs as give every active CTA the same number of items.
   static constexpr bool kBalanceRounds = TOK <= 64;
   static constexpr int kSub = TOK <= 224 ? TOK : 224;         // MMA N of one sub-tile (<= 256)
-  // SF slot: 4 weight-SF columns, then per sub-tile kSub/32 token-SF columns
+  // SF slot: 4 weight-SF columns per weight tile, then per sub-tile kSub/32 token-SF columns
   // starting every 8 columns (scale-factor TMEM addresses stay 4-column aligned)
   static constexpr int kSubSfCols = kSub / 32;
+  static constexpr int kWSfCols = 4 * WT;
   static constexpr int kSfCols = (kBf16 || kF32) ? 0 : kFp4 ? 32 : TOK <= 64 ? 8 : TOK <= 224 ? 16 : 32;
-  static __device__ __forceinline__ int tok_sf_col(int c) { return 4 + (c / kSubSfCols) * 8 + c % kSubSfCols; }
-  static constexpr int kSfBase = kAccBufs * TOK;
+  static __device__ __forceinline__ int tok_sf_col(int c) {
+    return kWSfCols + (c / kSubSfCols) * 8 + c % kSubSfCols;
+  }
+  static constexpr int kAccCols = WT * TOK;                   // one accumulator: WT blocks of TOK columns
+  static constexpr int kSfBase = kAccBufs * kAccCols;
   static constexpr int kTmemUsed = kSfBase + kSfSlots * kSfCols;
   static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
                                    : kTmemUsed <= 256 ? 256 : 512;
-  static constexpr int kStageB = kBlockW * kBlockK;           // bytes
+  static constexpr int kStageB = WT * kBlockW * kBlockK;      // bytes
   static constexpr int kStageA = TOK * kBlockK;
-  static constexpr int kEpiBytes = 4 * 32 * 32 * 2;           // per epilogue warp: 32 tokens x 32 columns bf16
+  // epilogue warps: one group of four (one per TMEM lane quadrant) per weight tile of the item, so
+  // with WT = 2 both halves of the accumulator drain at once (the next item's MMAs wait for them)
+  static constexpr int kEpiGroups = WT;
+  static constexpr int kEpiWarps = 4 * kEpiGroups;
+  // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue group 0, warps 6-9 SF loaders,
+  // warps 10.. further epilogue groups
+  static constexpr int kNumThreads = 32 * (2 + kEpiWarps + 4);
+  static constexpr int kEpiBytes = kEpiWarps * 32 * 32 * 2;   // per epilogue warp: 32 tokens x 32 columns bf16
   static constexpr int kTableBytes = (3 * MAXE + 4) * 4;
   static constexpr int kBarBytes = 512;
   // full + empty per stage, sf_full + sf_empty per SF slot, acc_full + acc_empty per accumulator,
@@ -135,7 +151,9 @@ struct Cfg {
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * (kStageB + kStageA + kStageSf) +
                                   kEpiBytes + kTableBytes + kBarBytes;
   static_assert(kSfBase + kSfSlots * kSfCols <= 512, "TMEM columns");
-  static_assert(kBf16 || kF32 || 4 + (TOK / kSub - 1) * 8 + kSubSfCols <= kSfCols, "SF slot width");
+  static_assert(kBf16 || kF32 || kWSfCols + (TOK / kSub - 1) * 8 + kSubSfCols <= kSfCols, "SF slot width");
+  static_assert(WT == 1 || (WT == 2 && FMT == kFmtFp8 && TOK == 224 && CPS == 1),
+                "two weight tiles per item: the FP8 224-token tile with one CTA per SM");
   static_assert(!kF32 || (TOK == 64 && CPS == 1) || (TOK == 32 && CPS == 2),
                 "FP32-scale tile: 64 tokens with one CTA per SM, or 32 with two (TOK FP32 accumulators per thread)");
   static_assert(kSubSfCols <= 8, "token SF columns of a sub-tile");
@@ -196,12 +214,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int TOK, int CPS, int MAXE, int FMT>
-__global__ void __launch_bounds__(kThreads, CPS)
+template <int TOK, int CPS, int MAXE, int FMT, int WT>
+__global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_sfb, const __grid_constant__ CUtensorMap tmap_sfa,
                         const GemmArgs p) {
-  using C = Cfg<TOK, CPS, MAXE, FMT>;
+  using C = Cfg<TOK, CPS, MAXE, FMT, WT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_b = smem;
@@ -225,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int E = p.E, N = p.N;
-  const int nnt = N / kBlockW;
+  const int nnt = N / kBlockW;                               // 128-row weight tiles per expert
+  const int nit = nnt / WT;                                  // work-item columns per token chunk
   const int nkb = p.K / C::kKElems;
   const int nw = C::kFp4 ? p.K / 64 : (nkb + 3) / 4;        // SF words per row
 
@@ -240,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
     }
     for (int s = 0; s < C::kAccBufs; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 4);
+      mbar_init(&acc_empty[s], C::kEpiWarps);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -278,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
         exp_row0[e] = row0;
         exp_cnt[e] = cnt;
       }
-      const int ntiles = ((cnt + TOK - 1) / TOK) * nnt;
+      const int ntiles = ((cnt + TOK - 1) / TOK) * nit;
       int incl = ntiles;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -314,18 +333,21 @@ __global__ void __launch_bounds__(kThreads, CPS)
       int issued = 0;
       bool ok = !(p.flags & BSF_DEBUG_WITHHOLD_LOADS);
       for (int t = t_first; t < total_tiles && ok; t += G) {
-        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
+        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nit, TOK);
         const int n_loads = (tl.ntok + C::kBoxRows - 1) / C::kBoxRows;
         const uint32_t bytes = C::kStageB + n_loads * C::kBoxRows * kBlockK + C::kSfStageBytes;
-        const int wrow = tl.e * N + tl.nt * kBlockW;
+        const int wt0 = tl.nt * WT;                          // first 128-row weight tile of the item
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], bytes);
-          if (p.flags & BSF_B_TILED)   // weights pre-tiled: box (e, nt, kb) is 16 KB contiguous
-            tma_load_2d(stage_b + stage * C::kStageB, &tmap_b, &full[stage], 0,
-                        ((tl.e * nnt + tl.nt) * nkb + kb) * kBlockW);
-          else
-            tma_load_2d(stage_b + stage * C::kStageB, &tmap_b, &full[stage], kb * kBlockK, wrow);
+#pragma unroll
+          for (int w = 0; w < WT; ++w) {
+            uint8_t* dst = stage_b + stage * C::kStageB + w * kBlockW * kBlockK;
+            if (p.flags & BSF_B_TILED)   // weights pre-tiled: box (e, weight tile, kb) is 16 KB contiguous
+              tma_load_2d(dst, &tmap_b, &full[stage], 0, ((tl.e * nnt + wt0 + w) * nkb + kb) * kBlockW);
+            else
+              tma_load_2d(dst, &tmap_b, &full[stage], kb * kBlockK, tl.e * N + (wt0 + w) * kBlockW);
+          }
           for (int i = 0; i < n_loads; ++i)
             tma_load_2d(stage_a + stage * C::kStageA + i * C::kBoxRows * kBlockK, &tmap_a, &full[stage],
                         kb * kBlockK, tl.tok0 + i * C::kBoxRows);
@@ -355,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int t = t_first; t < total_tiles && ok; t += G) {
-        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
+        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nit, TOK);
         const uint32_t mma_n = (tl.ntok + 15) & ~15;
         const uint32_t idesc = idesc_f8(kBlockW, mma_n);
         for (int kb = 0; kb < nkb; ++kb) {
@@ -378,11 +400,11 @@ __global__ void __launch_bounds__(kThreads, CPS)
       uint32_t stage = 0, phase = 0, sf_slot = 0, sf_phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int t = t_first; t < total_tiles && ok; t += G) {
-        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
+        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nit, TOK);
         const uint32_t mma_n = (tl.ntok + 15) & ~15;
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * TOK;
+        const uint32_t d_tmem = tmem_base + acc * C::kAccCols;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!C::kBf16 && kb % C::kKbPerSlot == 0) {
             if (!mbar_wait(&sf_full[sf_slot], sf_phase, abort_flag, p.err)) { ok = false; break; }
@@ -390,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
           if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sfw = tmem_base + C::kSfBase + sf_slot * C::kSfCols;
-          const uint32_t sft = sfw + 4;
+          const uint32_t sft = sfw + C::kWSfCols;
           const uint64_t adesc = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB));
           const uint64_t bdesc = smem_desc_k_sw128(smem_u32(stage_a + stage * C::kStageA));
           if constexpr (C::kFp4) {
@@ -417,10 +439,17 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 mma_bf16(d_tmem + j * C::kSub, adesc + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
             } else {
               const uint32_t idesc = idesc_mxf8_e4m3(kBlockW, nn, kb & 3, kb & 3);
+              uint64_t adw[WT];              // weight tile w of the stage; its accumulator block and SF columns
+#pragma unroll
+              for (int w = 0; w < WT; ++w)
+                adw[w] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + w * kBlockW * kBlockK));
 #pragma unroll
               for (int k = 0; k < kBlockK / 32; ++k) {
                 // advance 32 bytes (one K=32 step of FP8) inside the swizzled 128-byte rows
-                mma_mxf8(d_tmem + j * C::kSub, adesc + 2 * k, bd + 2 * k, idesc, sfw, sft + j * 8, (kb | k) != 0);
+#pragma unroll
+                for (int w = 0; w < WT; ++w)
+                  mma_mxf8(d_tmem + w * TOK + j * C::kSub, adw[w] + 2 * k, bd + 2 * k, idesc, sfw + 4 * w,
+                           sft + j * 8, (kb | k) != 0);
               }
             }
           }
@@ -441,10 +470,12 @@ __global__ void __launch_bounds__(kThreads, CPS)
       drain_wait(mma_done, 0);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 6 || warp >= 10) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // TMEM lane quadrant = weight rows 32q..32q+31
-    uint16_t* buf = reinterpret_cast<uint16_t*>(epi) + (warp - 2) * 32 * 32;
+    const int ew = warp < 6 ? warp - 2 : warp - 6;   // epilogue warp 0 .. kEpiWarps-1
+    const int group = ew / 4;                          // handles weight tiles group, group + kEpiGroups, ...
+    uint16_t* buf = reinterpret_cast<uint16_t*>(epi) + ew * 32 * 32;
     uint32_t acc = 0, acc_phase = 0;
     if constexpr (C::kF32) {
       // D[token, row] = sum_kb sB[e, nt, kb] * sA[token, kb] * partial_kb: promoted in FP32 registers,
@@ -452,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
       const int nnb = N / kBlockW;
       bool ok = true;
       for (int t = t_first; t < total_tiles && ok; t += G) {
-        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
+        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nit, TOK);
         float accv[TOK];
 #pragma unroll
         for (int j = 0; j < TOK; ++j) accv[j] = 0.f;
@@ -529,10 +560,10 @@ __global__ void __launch_bounds__(kThreads, CPS)
       }
     } else
     for (int t = t_first; t < total_tiles; t += G) {
-      const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
+      const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nit, TOK);
       if (!warp_wait(&acc_full[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * TOK;
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * C::kAccCols;
       const int ncol = (tl.ntok + 31) & ~31;
       // NVFP4: the tensor scales 2**a_exp * 2**b_exp[e], applied exactly (two power-of-two products)
       float alpha_a = 1.f, alpha_b = 1.f;
@@ -540,11 +571,15 @@ __global__ void __launch_bounds__(kThreads, CPS)
         alpha_a = exp2_int(p.a_exp);
         alpha_b = exp2_int(p.b_exp ? p.b_exp[tl.e] : 0);
       }
+      // weight tile w of the item: accumulator columns w * TOK.., output columns (nt * WT + w) * 128..
+      for (int w = group; w < WT; w += C::kEpiGroups) {
+      const uint32_t taddr = tacc + w * TOK;
+      const int64_t dcol = static_cast<int64_t>(tl.nt * WT + w) * kBlockW + 32 * q + (lane & 3) * 8;
       for (int c0 = 0; c0 < ncol; c0 += 32) {
         uint32_t r[32];
         tmem_ld_x32(taddr + c0, r);
         tmem_wait_ld();
-        if (c0 + 32 >= ncol) {            // last chunk is in registers: hand the accumulator back to the MMA issuer
+        if (w + C::kEpiGroups >= WT && c0 + 32 >= ncol) {   // last chunk in registers: hand the accumulator back
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -563,12 +598,12 @@ __global__ void __launch_bounds__(kThreads, CPS)
           const int j = (lane >> 2) + 8 * i;
           if (c0 + j < tl.ntok) {
             const uint4 v = *reinterpret_cast<const uint4*>(buf + j * 32 + (lane & 3) * 8);
-            uint16_t* dst = p.d + static_cast<int64_t>(tl.tok0 + c0 + j) * N + tl.nt * kBlockW + 32 * q +
-                            (lane & 3) * 8;
+            uint16_t* dst = p.d + static_cast<int64_t>(tl.tok0 + c0 + j) * N + dcol;
             *reinterpret_cast<uint4*>(dst) = v;
           }
         }
         __syncwarp();
+      }
       }
       if (ncol == 0) {
         tc_fence_before();
@@ -593,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
       // (one of the five arrivals on its empty barrier) as soon as the words are in registers.
       uint32_t stage = 0, phase = 0;
       for (int t = t_first; t < total_tiles && ok; t += G) {
-        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
+        const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nit, TOK);
         const int off = tl.tok0 & 3;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!warp_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
@@ -634,13 +669,17 @@ __global__ void __launch_bounds__(kThreads, CPS)
       }
     } else
     for (int t = t_first; t < total_tiles && ok; t += G) {
-      const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nnt, TOK);
+      const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nit, TOK);
       const int mma_n = (tl.ntok + 15) & ~15;
-      const int32_t* sfb_base = p.sfb + static_cast<int64_t>(tl.e) * nw * N + tl.nt * kBlockW + lane;
+      const int32_t* sfb_base = p.sfb + static_cast<int64_t>(tl.e) * nw * N + tl.nt * WT * kBlockW + lane;
       for (int g = 0; g < nw; ++g) {
-        uint32_t w[4];
+        uint32_t w[WT][4];             // weight tile w: rows lane + 32 c of the item's tile w
 #pragma unroll
-        for (int c = 0; c < 4; ++c) w[c] = static_cast<uint32_t>(__ldg(sfb_base + static_cast<int64_t>(g) * N + 32 * c));
+        for (int ww = 0; ww < WT; ++ww) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            w[ww][c] = static_cast<uint32_t>(__ldg(sfb_base + static_cast<int64_t>(g) * N + ww * kBlockW + 32 * c));
+        }
         uint32_t a[C::kTokSfCols];
 #pragma unroll
         for (int c = 0; c < C::kTokSfCols; ++c) {
@@ -652,7 +691,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
         if (!warp_wait(&sf_empty[sf_slot], sf_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t col = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::kSfBase + sf_slot * C::kSfCols;
-        tmem_st_x4(col, w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int ww = 0; ww < WT; ++ww) tmem_st_x4(col + 4 * ww, w[ww][0], w[ww][1], w[ww][2], w[ww][3]);
 #pragma unroll
         for (int c = 0; c < C::kTokSfCols; ++c) tmem_st_x1(col + C::tok_sf_col(c), a[c]);
         tmem_wait_st();
@@ -714,9 +754,9 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int TOK, int CPS = 1, int MAXE = kMaxExperts, int FMT = kFmtFp8>
+template <int TOK, int CPS = 1, int MAXE = kMaxExperts, int FMT = kFmtFp8, int WT = 1>
 bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int64_t max_tiles, cudaStream_t s) {
-  using C = Cfg<TOK, CPS, MAXE, FMT>;
+  using C = Cfg<TOK, CPS, MAXE, FMT, WT>;
   if (args.E > MAXE) return BSF_ERR_UNSUPPORTED;
   CUtensorMap map_a, map_b;
   const int64_t row_bytes = C::kFp4 ? args.K / 2 : C::kBf16 ? 2 * args.K : args.K;
@@ -738,10 +778,10 @@ bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int6
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<TOK, CPS, MAXE, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<TOK, CPS, MAXE, FMT, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::kSmem)) != cudaSuccess)
       return BSF_ERR_CUDA;
-    if (CPS > 1 && cudaFuncSetAttribute(grouped_gemm_kernel<TOK, CPS, MAXE, FMT>,
+    if (CPS > 1 && cudaFuncSetAttribute(grouped_gemm_kernel<TOK, CPS, MAXE, FMT, WT>,
                                         cudaFuncAttributePreferredSharedMemoryCarveout,
                                         cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return BSF_ERR_CUDA;
@@ -751,9 +791,9 @@ bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int6
   if (max_tiles < grid) grid = max_tiles;
   if (grid <= 0) return BSF_OK;
   if (C::kDependentLaunch)
-    return launch_dependent(grouped_gemm_kernel<TOK, CPS, MAXE, FMT>, static_cast<unsigned>(grid), kThreads, C::kSmem, s,
+    return launch_dependent(grouped_gemm_kernel<TOK, CPS, MAXE, FMT, WT>, static_cast<unsigned>(grid), C::kNumThreads, C::kSmem, s,
                             map_b, map_a, map_sfb, map_sfa, args);
-  grouped_gemm_kernel<TOK, CPS, MAXE, FMT><<<static_cast<unsigned>(grid), kThreads, C::kSmem, s>>>(
+  grouped_gemm_kernel<TOK, CPS, MAXE, FMT, WT><<<static_cast<unsigned>(grid), C::kNumThreads, C::kSmem, s>>>(
       map_b, map_a, map_sfb, map_sfa, args);
   return launch_status();
 }
@@ -817,6 +857,10 @@ extern "C" bsf_status bsf_grouped_gemm_contig(const uint8_t* a, const int32_t* s
     const int64_t max_tiles = (m_cap / kHostTok + E) * (N / 128);
     return launch<kHostTok>(args, a, b, max_tiles, s);
   }
+  if (N % 256 == 0) {   // 256 x 224 items (two weight tiles), one CTA per SM
+    const int64_t max_items = (m_cap / kBigTok + E) * (N / 256);
+    return launch<kBigTok, 1, kMaxExperts, kFmtFp8, 2>(args, a, b, max_items, s);
+  }
   const int64_t max_tiles = (m_cap / kBigTok + E) * (N / 128);
   return launch<kBigTok, 2>(args, a, b, max_tiles, s);
 }
@@ -849,6 +893,10 @@ extern "C" bsf_status bsf_grouped_gemm_masked(const uint8_t* a, const int32_t* s
   if (host && max_m > kBigTok) {
     const int64_t max_tiles = E * ((max_m + kHostTok - 1) / kHostTok) * (N / 128);
     return launch<kHostTok>(args, a, b, max_tiles, s);
+  }
+  if (N % 256 == 0) {
+    const int64_t max_items = E * ((max_m + kBigTok - 1) / kBigTok) * (N / 256);
+    return launch<kBigTok, 1, kMaxExperts, kFmtFp8, 2>(args, a, b, max_items, s);
   }
   const int64_t max_tiles = E * ((max_m + kBigTok - 1) / kBigTok) * (N / 128);
   return launch<kBigTok, 2>(args, a, b, max_tiles, s);
