@@ -44,6 +44,7 @@ constexpr int kFmtNvfp4 = 1;        // E2M1 operands, UE4M3 scales per 16 K (kin
 constexpr int kFmtBf16 = 2;         // BF16 operands, no scales (kind::f16)
 constexpr int kFmtFp8F32 = 3;       // E4M3 operands, float32 scales applied in software per 128-K block
 constexpr int kNvfp4MaxE = 256;     // NVFP4 variants size their tile tables for 256 experts
+constexpr int kPrefetchStages = 12; // weight stages a dependent small-batch CTA pulls into L2 before its wait
 
 struct GemmArgs {
   const int32_t* seg_start;  // contiguous: [E+1]; masked: nullptr
@@ -271,8 +272,25 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
       tma_prefetch_desc(&tmap_sfa);
     }
   }
+  // Dependent launch: the weights are not written by the preceding kernel, so while it drains,
+  // start pulling into L2 the first stages of the tile this CTA most likely takes first (tile
+  // blockIdx.x when every expert holds one token chunk, as at decode).  A wrong guess costs only
+  // bandwidth.  Weights in host memory are left alone (every byte crosses the host link).
+  if (C::kDependentLaunch && warp == 0 && lane == 0 && !(p.flags & BSF_B_HOST_MAPPED)) {
+    const int e = static_cast<int>(blockIdx.x) / nnt, nt = static_cast<int>(blockIdx.x) % nnt;
+    if (e < E) {
+      const int n_pf = nkb < kPrefetchStages ? nkb : kPrefetchStages;
+      for (int kb = 0; kb < n_pf; ++kb) {
+        if (p.flags & BSF_B_TILED)
+          tma_prefetch_l2(&tmap_b, 0, ((e * nnt + nt) * nkb + kb) * kBlockW);
+        else
+          tma_prefetch_l2(&tmap_b, kb * kBlockK, e * N + nt * kBlockW);
+      }
+    }
+  }
   // when launched as a dependent, everything above overlaps the tail of the preceding kernel;
-  // no global memory and no tensor memory is touched before it has completed (no-op otherwise)
+  // nothing the preceding kernel writes, and no tensor memory, is touched before it has completed
+  // (no-op otherwise)
   pdl_wait();
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);

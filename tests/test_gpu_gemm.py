@@ -70,11 +70,13 @@ def test_contig_ragged_segments(dev, K, align):
         assert np.isnan(dv[seg[e] + counts[e]:seg[e + 1]]).all()
 
 
-@pytest.mark.parametrize("max_m,expected_m", [(64, 0), (320, 0), (320, 16)])
-def test_masked_ragged(dev, max_m, expected_m):
+@pytest.mark.parametrize("max_m,expected_m,N", [(64, 0, 384), (320, 0, 384), (320, 16, 384), (320, 0, 512),
+                                                 (128, 0, 512)])
+def test_masked_ragged(dev, max_m, expected_m, N):
+    """N = 384: 128-row weight tiles; N = 512: 256-row work items (two weight tiles per token chunk)."""
     masked = np.array([0, 1, 16, 63, 64, max_m // 2, max_m, 7])
     masked = np.minimum(masked, max_m)
-    E, N, K = len(masked), 384, 512
+    E, K = len(masked), 512
     (aq, asf, bq, sfb), ref_ops = _operands(E * max_m, E, N, K, max_m + expected_m, dev)
     d = torch.full((E * max_m, N), float("nan"), dtype=torch.bfloat16, device=dev)
     ops.grouped_gemm_masked(aq, asf, bq, sfb, torch.as_tensor(masked, dtype=torch.int32, device=dev), max_m,
@@ -97,6 +99,22 @@ def test_masked_many_experts_small_slots(dev):
     torch.cuda.synchronize()
     assert ops.device_error() == 0
     _check_all(d, ref_ops, np.arange(E + 1) * max_m, masked, "masked E=260")
+
+
+def test_contig_many_experts_wide_items(dev):
+    """More than 256 experts with 256-row work items (the 1024-expert tile tables)."""
+    rng = np.random.default_rng(12)
+    E, N, K = 260, 256, 256
+    counts = rng.integers(0, 40, E)
+    counts[::7] = 0
+    seg = np.concatenate([[0], np.cumsum(counts)])
+    (aq, asf, bq, sfb), ref_ops = _operands(int(seg[-1]), E, N, K, 78, dev)
+    d = torch.full((int(seg[-1]), N), float("nan"), dtype=torch.bfloat16, device=dev)
+    ops.grouped_gemm_contig(aq, asf, bq, sfb, torch.as_tensor(seg, dtype=torch.int32, device=dev),
+                            torch.as_tensor(counts, dtype=torch.int32, device=dev), d=d)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    _check_all(d, ref_ops, seg, counts, "contig E=260 wide items")
 
 
 def test_grouped_equals_single_launches_bitwise(dev):

@@ -41,9 +41,9 @@ def _problem(E, N, K, rows, seed, dev):
     return x, w, aq, asf, bq, sfb
 
 
-@pytest.mark.parametrize("max_m", [64, 320])
-def test_masked_host_weights_bitwise_equal_to_hbm_weights(dev, max_m):
-    E, N, K = 6, 384, 1024
+@pytest.mark.parametrize("max_m,N", [(64, 384), (320, 384), (128, 512)])
+def test_masked_host_weights_bitwise_equal_to_hbm_weights(dev, max_m, N):
+    E, K = 6, 1024
     masked = np.minimum(np.array([0, 3, 17, 64, 200, max_m]), max_m)
     x, w, aq, asf, bq, sfb = _problem(E, N, K, E * max_m, max_m, dev)
     mm = torch.as_tensor(masked, dtype=torch.int32, device=dev)
