@@ -14,10 +14,15 @@
 // * swap-AB: the MMA's M = 128 rows are WEIGHT rows (an N-tile of the output)
 //   and the MMA's N dimension is the expert's TOKENS (16..256, step 16), so
 //   a segment of 8 tokens costs a 128 x 16 MMA instead of a padded 128 x 128;
-// * one CTA per SM, persistent; work item = (expert, N-tile, token chunk),
-//   chunks fastest so concurrent CTAs share the weight tile in L2;
+// * persistent CTAs (one or two per SM); work item = (expert, N-tile, token
+//   chunk), chunks fastest so concurrent CTAs share the weight tile in L2;
+//   large FP8 batches take 256-row items (two 128-row weight tiles sharing
+//   one token chunk, one MMA per weight tile per K-step);
 // * warp roles: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner,
-//   warps 2-5 epilogue, warps 6-9 scale-factor loaders;
+//   warps 2-5 epilogue, warps 6-9 scale-factor loaders (warps 10-13: a
+//   second epilogue group for the 256-row items);
+// * weights either row-major [E, N, K] or tiled (each 128 x 128-byte TMA box
+//   one contiguous 16 KB run, BSF_B_TILED);
 // * operands: K-major, 128-byte swizzled tiles of 128 K (TMA), STAGES-deep
 //   mbarrier ring; accumulator 128 lanes x TOK fp32 columns in TMEM;
 // * scales: kind::mxf8f6f4 block scaling with one UE8M0 per row per 32 K;
