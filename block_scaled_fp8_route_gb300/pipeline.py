@@ -189,6 +189,10 @@ class MoEPath:
         """
         self.step(x, topk_ids, topk_weights, h2)
         torch.cuda.synchronize()
+        # the graph reads these tensors' memory on every replay: keep them alive with it (torch
+        # releases cached blocks to the driver when a capture begins, so a dropped input would
+        # leave the graph pointing at unmapped memory)
+        self._graph_inputs = (x, topk_ids, topk_weights, h2)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             self.step(x, topk_ids, topk_weights, h2)

@@ -95,6 +95,8 @@ def test_graph_replay_matches_eager_step(dev, name):
     path = MoEPath(w.E, w.kr, w.T, w.K, w.N, wt, layout=w.layout, align_or_max_m=a_or_m, device=dev)
     eager = path.step(x, ids, p).clone()
     path.capture(x, ids, p)
+    # the graph holds its input tensors, so a caller dropping them cannot free memory it reads
+    assert path._graph_inputs[0] is x and path._graph_inputs[1] is ids and path._graph_inputs[2] is p
     for _ in range(3):
         assert torch.equal(path.replay().view(torch.int16), eager.view(torch.int16))
     # new inputs written into the captured buffers are picked up by the replay
