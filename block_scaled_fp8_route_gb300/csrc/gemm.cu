@@ -143,11 +143,15 @@ struct Cfg {
   static constexpr int kStageA = TOK * kBlockK;
   // epilogue warps: one group of four (one per TMEM lane quadrant) per weight tile of the item, so
   // with WT = 2 both halves of the accumulator drain at once (the next item's MMAs wait for them)
-  static constexpr int kEpiGroups = WT;
+  // FP32 scales with 128-token tiles: two groups of four epilogue warps each promote 64 of the
+  // tile's token columns (64 FP32 accumulators per thread); the second group is warps 6-9, which
+  // load no scale factors in this format
+  static constexpr bool kF32Wide = kF32 && TOK == 128;
+  static constexpr int kEpiGroups = (kF32Wide || WT == 2) ? 2 : 1;
   static constexpr int kEpiWarps = 4 * kEpiGroups;
-  // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue group 0, warps 6-9 SF loaders,
-  // warps 10.. further epilogue groups
-  static constexpr int kNumThreads = 32 * (2 + kEpiWarps + 4);
+  // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue group 0, warps 6-9 SF loaders
+  // (epilogue group 1 when kF32Wide), warps 10.. further epilogue groups
+  static constexpr int kNumThreads = kF32Wide ? 320 : 32 * (2 + kEpiWarps + 4);
   static constexpr int kEpiBytes = kEpiWarps * 32 * 32 * 2;   // per epilogue warp: 32 tokens x 32 columns bf16
   static constexpr int kTableBytes = (3 * MAXE + 4) * 4;
   static constexpr int kBarBytes = 512;
@@ -160,8 +164,9 @@ struct Cfg {
   static_assert(kBf16 || kF32 || kWSfCols + (TOK / kSub - 1) * 8 + kSubSfCols <= kSfCols, "SF slot width");
   static_assert(WT == 1 || (WT == 2 && FMT == kFmtFp8 && TOK == 224 && CPS == 1),
                 "two weight tiles per item: the FP8 224-token tile with one CTA per SM");
-  static_assert(!kF32 || (TOK == 64 && CPS == 1) || (TOK == 32 && CPS == 2),
-                "FP32-scale tile: 64 tokens with one CTA per SM, or 32 with two (TOK FP32 accumulators per thread)");
+  static_assert(!kF32 || ((TOK == 64 || TOK == 128) && CPS == 1) || (TOK == 32 && CPS == 2),
+                "FP32-scale tile: 64 or 128 tokens with one CTA per SM, or 32 with two (at most 64 FP32 "
+                "accumulators per thread)");
   static_assert(kSubSfCols <= 8, "token SF columns of a sub-tile");
   static_assert(kTmemUsed <= 512, "TMEM budget");
   static_assert(kSmem * CPS + 1024 * CPS <= 233472, "shared memory budget");
@@ -493,10 +498,10 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
       drain_wait(mma_done, 0);
     }
     __syncwarp();
-  } else if (warp < 6 || warp >= 10) {
+  } else if (warp < 6 || warp >= 10 || (C::kF32Wide && warp < 10)) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // TMEM lane quadrant = weight rows 32q..32q+31
-    const int ew = warp < 6 ? warp - 2 : warp - 6;   // epilogue warp 0 .. kEpiWarps-1
+    const int ew = warp < 10 ? warp - 2 : warp - 6;  // epilogue warp 0 .. kEpiWarps-1
     const int group = ew / 4;                          // handles weight tiles group, group + kEpiGroups, ...
     uint16_t* buf = reinterpret_cast<uint16_t*>(epi) + ew * 32 * 32;
     uint32_t acc = 0, acc_phase = 0;
@@ -507,11 +512,14 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
       bool ok = true;
       for (int t = t_first; t < total_tiles && ok; t += G) {
         const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nit, TOK);
-        float accv[TOK];
+        // this warp group's token columns gt0 .. gt0 + kGT - 1 of the tile
+        constexpr int kGT = TOK / C::kEpiGroups;
+        const int gt0 = group * kGT;
+        float accv[kGT];
 #pragma unroll
-        for (int j = 0; j < TOK; ++j) accv[j] = 0.f;
+        for (int j = 0; j < kGT; ++j) accv[j] = 0.f;
         const float* sbp = p.sfb_f32 + (static_cast<int64_t>(tl.e) * nnb + tl.nt) * nkb;
-        const int64_t r0 = static_cast<int64_t>(tl.tok0) + lane;
+        const int64_t r0 = static_cast<int64_t>(tl.tok0) + gt0 + lane;
         // the scales of K-blocks kb .. kb+3 are in flight ahead of their partials (a queue in registers)
         float qb[4], q0[4], q1[4];
         auto fetch = [&](int kk, float& b, float& s0, float& s1) {
@@ -519,8 +527,8 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
           if (kk < nkb) {
             const float* sap = p.sfa_f32 + static_cast<int64_t>(kk) * p.sfa_ld;
             b = __ldg(sbp + kk);
-            if (lane < tl.ntok) s0 = __ldg(sap + r0);
-            if (lane + 32 < tl.ntok) s1 = __ldg(sap + r0 + 32);
+            if (gt0 + lane < tl.ntok) s0 = __ldg(sap + r0);
+            if (gt0 + lane + 32 < tl.ntok) s1 = __ldg(sap + r0 + 32);
           }
         };
 #pragma unroll
@@ -536,15 +544,17 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
           fetch(kb + 4, qb[3], q0[3], q1[3]);
           if (!warp_wait(&acc_full[acc], acc_phase, abort_flag, p.err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * TOK;
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * TOK + gt0;
           uint32_t r[32];
-          tmem_ld_x32(taddr, r);
-          tmem_wait_ld();
+          if (gt0 < tl.ntok) {
+            tmem_ld_x32(taddr, r);
+            tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            accv[j] = fmaf(__uint_as_float(r[j]), sb * __shfl_sync(0xffffffffu, sa0, j), accv[j]);
-          if constexpr (TOK > 32) {
-          if (tl.ntok > 32) {
+            for (int j = 0; j < 32; ++j)
+              accv[j] = fmaf(__uint_as_float(r[j]), sb * __shfl_sync(0xffffffffu, sa0, j), accv[j]);
+          }
+          if constexpr (kGT > 32) {
+          if (tl.ntok > gt0 + 32) {
             tmem_ld_x32(taddr + 32, r);
             tmem_wait_ld();
 #pragma unroll
@@ -559,12 +569,12 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
         }
         if (!ok) break;
 #pragma unroll
-        for (int half = 0; half < TOK / 32; ++half) {
-          const int c0 = 32 * half;
+        for (int half = 0; half < kGT / 32; ++half) {
+          const int c0 = gt0 + 32 * half;             // token column of the tile
           if (c0 >= tl.ntok) break;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const __nv_bfloat16 h = __float2bfloat16_rn(accv[c0 + j]);
+            const __nv_bfloat16 h = __float2bfloat16_rn(accv[32 * half + j]);
             buf[j * 32 + lane] = *reinterpret_cast<const uint16_t*>(&h);
           }
           __syncwarp();
@@ -1082,8 +1092,9 @@ extern "C" bsf_status bsf_grouped_gemm_f32sf_contig(const uint8_t* a, const floa
   GemmArgs args{seg_start, counts, 0, m_cap, nullptr, sfa_ld, nullptr, static_cast<uint16_t*>(d),
                 static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
                 flags, 0, nullptr, sfa, reinterpret_cast<const float*>(sfb_i)};
-  const int64_t max_tiles = (m_cap / 64 + E) * (N / 128);
-  return launch<64, 1, kMaxExperts, kFmtFp8F32>(args, a, b, max_tiles, reinterpret_cast<cudaStream_t>(stream));
+  // 128-token tiles: each weight tile is streamed once per 128 rows of an expert
+  const int64_t max_tiles = (m_cap / 128 + E) * (N / 128);
+  return launch<128, 1, kMaxExperts, kFmtFp8F32>(args, a, b, max_tiles, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" bsf_status bsf_grouped_gemm_f32sf_masked(const uint8_t* a, const float* sfa, int64_t sfa_ld,
@@ -1112,6 +1123,10 @@ extern "C" bsf_status bsf_grouped_gemm_f32sf_masked(const uint8_t* a, const floa
     if (E <= 256) return launch<32, 2, 256, kFmtFp8F32>(args, a, b, max_tiles, s);
     return launch<32, 2, kMaxExperts, kFmtFp8F32>(args, a, b, max_tiles, s);
   }
-  const int64_t max_tiles = E * ((max_m + 63) / 64) * (N / 128);
-  return launch<64, 1, kMaxExperts, kFmtFp8F32>(args, a, b, max_tiles, s);
+  if (max_m <= 64 || hint <= 64) {
+    const int64_t max_tiles = E * ((max_m + 63) / 64) * (N / 128);
+    return launch<64, 1, kMaxExperts, kFmtFp8F32>(args, a, b, max_tiles, s);
+  }
+  const int64_t max_tiles = E * ((max_m + 127) / 128) * (N / 128);
+  return launch<128, 1, kMaxExperts, kFmtFp8F32>(args, a, b, max_tiles, s);
 }
