@@ -87,7 +87,7 @@ struct GemmArgs {
 // scale words cover four stages (one byte per stage, picked by sf_id);
 // NVFP4 needs a word per row per MMA, so its SF slot covers one stage:
 // 4 x 4 weight columns + 4 x 4 token columns (tokens <= 128).
-// WT = weight tiles per work item.  WT = 2 (FP8, 224 tokens, one CTA per SM): a stage holds two
+// WT = weight tiles per work item.  WT = 2 (FP8 or BF16, 224 tokens, one CTA per SM): a stage holds two
 // 128-row weight tiles and one token tile, and each K-step issues one MMA per weight tile into its
 // own 224-column accumulator, so a work item is a 256 x 224 output block.  The bytes a stage brings
 // into shared memory then cover 1.47x the MMA work of the 128 x 224 tile ((256 + 224) bytes per
@@ -162,8 +162,8 @@ struct Cfg {
                                   kEpiBytes + kTableBytes + kBarBytes;
   static_assert(kSfBase + kSfSlots * kSfCols <= 512, "TMEM columns");
   static_assert(kBf16 || kF32 || kWSfCols + (TOK / kSub - 1) * 8 + kSubSfCols <= kSfCols, "SF slot width");
-  static_assert(WT == 1 || (WT == 2 && FMT == kFmtFp8 && TOK == 224 && CPS == 1),
-                "two weight tiles per item: the FP8 224-token tile with one CTA per SM");
+  static_assert(WT == 1 || (WT == 2 && (FMT == kFmtFp8 || FMT == kFmtBf16) && TOK == 224 && CPS == 1),
+                "two weight tiles per item: the FP8 or BF16 224-token tile with one CTA per SM");
   static_assert(!kF32 || ((TOK == 64 || TOK == 128) && CPS == 1) || (TOK == 32 && CPS == 2),
                 "FP32-scale tile: 64 or 128 tokens with one CTA per SM, or 32 with two (at most 64 FP32 "
                 "accumulators per thread)");
@@ -462,9 +462,16 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
             if constexpr (C::kBf16) {
               // four K = 16 steps of 32 bytes inside the swizzled 128-byte rows
               const uint32_t idesc = idesc_bf16(kBlockW, nn);
+              uint64_t adw[WT];
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_bf16(d_tmem + j * C::kSub, adesc + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+              for (int w = 0; w < WT; ++w)
+                adw[w] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + w * kBlockW * kBlockK));
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                for (int w = 0; w < WT; ++w)
+                  mma_bf16(d_tmem + w * TOK + j * C::kSub, adw[w] + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+              }
             } else {
               const uint32_t idesc = idesc_mxf8_e4m3(kBlockW, nn, kb & 3, kb & 3);
               uint64_t adw[WT];              // weight tile w of the stage; its accumulator block and SF columns
@@ -1034,6 +1041,10 @@ extern "C" bsf_status bsf_grouped_gemm_bf16_contig(const void* a, int64_t m_cap,
     const int64_t max_tiles = (m_cap / kHostTok + E) * (N / 128);
     return launch<kHostTok, 1, kMaxExperts, kFmtBf16>(args, ad, bd, max_tiles, s);
   }
+  if (N % 256 == 0) {   // 256 x 224 items (two weight tiles), one CTA per SM
+    const int64_t max_items = (m_cap / kBigTok + E) * (N / 256);
+    return launch<kBigTok, 1, kMaxExperts, kFmtBf16, 2>(args, ad, bd, max_items, s);
+  }
   const int64_t max_tiles = (m_cap / kBigTok + E) * (N / 128);
   return launch<kBigTok, 2, kMaxExperts, kFmtBf16>(args, ad, bd, max_tiles, s);
 }
@@ -1064,6 +1075,10 @@ extern "C" bsf_status bsf_grouped_gemm_bf16_masked(const void* a, const void* b,
   if (host && max_m > kBigTok) {
     const int64_t max_tiles = E * ((max_m + kHostTok - 1) / kHostTok) * (N / 128);
     return launch<kHostTok, 1, kMaxExperts, kFmtBf16>(args, ad, bd, max_tiles, s);
+  }
+  if (N % 256 == 0) {
+    const int64_t max_items = E * ((max_m + kBigTok - 1) / kBigTok) * (N / 256);
+    return launch<kBigTok, 1, kMaxExperts, kFmtBf16, 2>(args, ad, bd, max_items, s);
   }
   const int64_t max_tiles = E * ((max_m + kBigTok - 1) / kBigTok) * (N / 128);
   return launch<kBigTok, 2, kMaxExperts, kFmtBf16>(args, ad, bd, max_tiles, s);
