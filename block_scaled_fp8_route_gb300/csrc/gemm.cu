@@ -110,7 +110,7 @@ struct Cfg {
   // NVFP4 scale words of one stage in shared memory: weights [4 MMAs][128 rows] int32 (box 128 x 4),
   // tokens [4 MMAs][TOK + 4] int32 (box TOK + 4 wide from the 4-aligned row at or below the tile's first)
   static constexpr int kSfTokCols = TOK + 4;
-  static constexpr int kSfStageBytes = kFp4 ? 4 * kBlockW * 4 + 4 * kSfTokCols * 4 : 0;
+  static constexpr int kSfStageBytes = kFp4 ? 4 * kBlockW * 4 * WT + 4 * kSfTokCols * 4 : 0;
   static constexpr int kStageSf = (kSfStageBytes + 127) / 128 * 128;
   static constexpr int kAccBufs = kF32 ? 4 : (CPS == 1 && TOK <= 224 && WT == 1) ? 2 : 1;
   static constexpr int kSfSlots = (kBf16 || kF32) ? 1 : kFp4 ? 4 : (CPS == 1 && TOK <= 224 && WT == 1) ? 4 : 2;
@@ -130,7 +130,8 @@ struct Cfg {
   // starting every 8 columns (scale-factor TMEM addresses stay 4-column aligned)
   static constexpr int kSubSfCols = kSub / 32;
   static constexpr int kWSfCols = 4 * WT;
-  static constexpr int kSfCols = (kBf16 || kF32) ? 0 : kFp4 ? 32 : TOK <= 64 ? 8 : TOK <= 224 ? 16 : 32;
+  // NVFP4 slot: 16 weight-SF columns per weight tile (four MMAs x four), then 16 token-SF columns
+  static constexpr int kSfCols = (kBf16 || kF32) ? 0 : kFp4 ? 16 * WT + 16 : TOK <= 64 ? 8 : TOK <= 224 ? 16 : 32;
   static __device__ __forceinline__ int tok_sf_col(int c) {
     return kWSfCols + (c / kSubSfCols) * 8 + c % kSubSfCols;
   }
@@ -162,8 +163,9 @@ struct Cfg {
                                   kEpiBytes + kTableBytes + kBarBytes;
   static_assert(kSfBase + kSfSlots * kSfCols <= 512, "TMEM columns");
   static_assert(kBf16 || kF32 || kWSfCols + (TOK / kSub - 1) * 8 + kSubSfCols <= kSfCols, "SF slot width");
-  static_assert(WT == 1 || (WT == 2 && (FMT == kFmtFp8 || FMT == kFmtBf16) && TOK == 224 && CPS == 1),
-                "two weight tiles per item: the FP8 or BF16 224-token tile with one CTA per SM");
+  static_assert(WT == 1 || (WT == 2 && CPS == 1 && (((FMT == kFmtFp8 || FMT == kFmtBf16) && TOK == 224) ||
+                                                    (FMT == kFmtNvfp4 && TOK == 128))),
+                "two weight tiles per item, one CTA per SM: FP8 or BF16 with 224 tokens, NVFP4 with 128");
   static_assert(!kF32 || ((TOK == 64 || TOK == 128) && CPS == 1) || (TOK == 32 && CPS == 2),
                 "FP32-scale tile: 64 or 128 tokens with one CTA per SM, or 32 with two (at most 64 FP32 "
                 "accumulators per thread)");
@@ -383,8 +385,11 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
             // scale words of MMAs 4kb .. 4kb+3: weight rows of the tile, and the tile's token rows
             // from the 4-aligned row at or below tok0 (the x coordinate of a TMA copy must be 16-byte aligned)
             uint8_t* sf_dst = stage_sf + stage * C::kStageSf;
-            tma_load_2d(sf_dst, &tmap_sfb, &full[stage], tl.nt * kBlockW, tl.e * nw + kb * 4);
-            tma_load_2d(sf_dst + 4 * kBlockW * 4, &tmap_sfa, &full[stage], tl.tok0 & ~3, kb * 4);
+#pragma unroll
+            for (int w = 0; w < WT; ++w)
+              tma_load_2d(sf_dst + w * 4 * kBlockW * 4, &tmap_sfb, &full[stage], (tl.nt * WT + w) * kBlockW,
+                          tl.e * nw + kb * 4);
+            tma_load_2d(sf_dst + WT * 4 * kBlockW * 4, &tmap_sfa, &full[stage], tl.tok0 & ~3, kb * 4);
           }
           ++issued;
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -447,10 +452,19 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
             // four K = 64 steps; step k's scales: weight words at columns 4k, token words at 16 + 4k
             // (NVFP4 tiles hold at most 128 tokens: one sub-tile, MMA N = mma_n <= 128)
             static_assert(!C::kFp4 || TOK == C::kSub, "NVFP4: one MMA sub-tile");
+            // (two weight tiles: tile w's words at 16 w + 4k, token words at 16 WT + 4k)
             const uint32_t idesc = idesc_nvf4(kBlockW, mma_n);
+            uint64_t adw[WT];
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_nvf4(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sfw + 4 * k, sfw + 16 + 4 * k, (kb | k) != 0);
+            for (int w = 0; w < WT; ++w)
+              adw[w] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + w * kBlockW * kBlockK));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+#pragma unroll
+              for (int w = 0; w < WT; ++w)
+                mma_nvf4(d_tmem + w * TOK, adw[w] + 2 * k, bdesc + 2 * k, idesc, sfw + 16 * w + 4 * k,
+                         sfw + 16 * WT + 4 * k, (kb | k) != 0);
+            }
           } else {
           // sub-tiles of at most kSub tokens: columns j*kSub.., smem rows j*kSub.., token SF columns j*kSub/32..
 #pragma unroll
@@ -673,13 +687,16 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
         for (int kb = 0; kb < nkb; ++kb) {
           if (!warp_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
           const uint32_t* sw = reinterpret_cast<const uint32_t*>(stage_sf + stage * C::kStageSf);
-          const uint32_t* st = sw + 4 * kBlockW;
-          uint32_t w[4][4];
+          const uint32_t* st = sw + 4 * kBlockW * WT;
+          uint32_t w[WT][4][4];            // weight tile ww, MMA k, rows lane + 32 c
           uint32_t a[4][C::kTokSfCols];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) w[k][c] = sw[k * kBlockW + 32 * c + lane];
+            for (int ww = 0; ww < WT; ++ww) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) w[ww][k][c] = sw[(ww * 4 + k) * kBlockW + 32 * c + lane];
+            }
 #pragma unroll
             for (int c = 0; c < C::kTokSfCols; ++c) {
               const int rl = lane + 32 * c;
@@ -694,11 +711,15 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
           const uint32_t col =
               tmem_base + (static_cast<uint32_t>(32 * q) << 16) + C::kSfBase + sf_slot * C::kSfCols;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) tmem_st_x4(col + 4 * k, w[k][0], w[k][1], w[k][2], w[k][3]);
+          for (int ww = 0; ww < WT; ++ww) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tmem_st_x4(col + 16 * ww + 4 * k, w[ww][k][0], w[ww][k][1], w[ww][k][2], w[ww][k][3]);
+          }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
 #pragma unroll
-            for (int c = 0; c < C::kTokSfCols; ++c) tmem_st_x1(col + 16 + 4 * k + c, a[k][c]);
+            for (int c = 0; c < C::kTokSfCols; ++c) tmem_st_x1(col + 16 * WT + 4 * k + c, a[k][c]);
           }
           tmem_wait_st();
           tc_fence_before();
@@ -962,6 +983,10 @@ extern "C" bsf_status bsf_grouped_gemm_nvfp4_contig(const uint8_t* a, const int3
   GemmArgs args{seg_start, counts, 0, m_cap, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
                 static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
                 flags, a_exp, b_exp};
+  if (N % 256 == 0) {   // 256 x 128 items (two weight tiles), one CTA per SM
+    const int64_t max_items = (m_cap / 128 + E) * (N / 256);
+    return launch<128, 1, kNvfp4MaxE, kFmtNvfp4, 2>(args, a, b, max_items, reinterpret_cast<cudaStream_t>(stream));
+  }
   const int64_t max_tiles = (m_cap / 128 + E) * (N / 128);
   return launch<128, 2, kNvfp4MaxE, kFmtNvfp4>(args, a, b, max_tiles, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -988,6 +1013,10 @@ extern "C" bsf_status bsf_grouped_gemm_nvfp4_masked(const uint8_t* a, const int3
   if (max_m <= 64 || ((flags & BSF_B_HOST_MAPPED) == 0 && hint <= 32)) {
     const int64_t max_tiles = E * ((max_m + 63) / 64) * (N / 128);
     return launch<64, 2, kNvfp4MaxE, kFmtNvfp4>(args, a, b, max_tiles, s);
+  }
+  if (N % 256 == 0) {
+    const int64_t max_items = E * ((max_m + 127) / 128) * (N / 256);
+    return launch<128, 1, kNvfp4MaxE, kFmtNvfp4, 2>(args, a, b, max_items, s);
   }
   const int64_t max_tiles = E * ((max_m + 127) / 128) * (N / 128);
   return launch<128, 2, kNvfp4MaxE, kFmtNvfp4>(args, a, b, max_tiles, s);

@@ -109,13 +109,14 @@ def test_masked_gemm(dev, max_m, expected_m):
     _check(d, ref_ops, np.arange(E + 1) * max_m, masked, f"nvfp4 masked max_m={max_m}")
 
 
-@pytest.mark.parametrize("align", [1, 128])
-def test_contig_gemm_ragged(dev, align):
+@pytest.mark.parametrize("align,N", [(1, 384), (128, 384), (1, 512)])
+def test_contig_gemm_ragged(dev, align, N):
+    """N = 384: 128-row weight tiles; N = 512: 256-row work items (two weight tiles per token chunk)."""
     counts = np.array([1, 15, 16, 17, 31, 33, 0, 129, 250, 3])
-    E, N, K = len(counts), 384, 768
+    E, K = len(counts), 768
     seg = np.concatenate([[0], np.cumsum((counts + align - 1) // align * align)])
     rows = int(seg[-1])
-    ops_, ref_ops = _gemm_operands(rows, E, N, K, 20 + align, dev)
+    ops_, ref_ops = _gemm_operands(rows, E, N, K, 20 + align + N, dev)
     aq, asf, bq, sfb, b_exp = ops_
     d = torch.full((rows, N), float("nan"), dtype=torch.bfloat16, device=dev)
     ops.grouped_gemm_nvfp4_contig(aq, asf, 0, bq, sfb, b_exp, torch.as_tensor(seg, dtype=torch.int32, device=dev),
