@@ -113,10 +113,14 @@ struct Cfg {
   static constexpr int kSfStageBytes = kFp4 ? 4 * kBlockW * 4 * WT + 4 * kSfTokCols * 4 : 0;
   static constexpr int kStageSf = (kSfStageBytes + 127) / 128 * 128;
   static constexpr int kAccBufs = kF32 ? 4 : (CPS == 1 && TOK <= 224 && WT == 1) ? 2 : 1;
-  static constexpr int kSfSlots = (kBf16 || kF32) ? 1 : kFp4 ? 4 : (CPS == 1 && TOK <= 224 && WT == 1) ? 4 : 2;
   static constexpr int kTokSfCols = (TOK + 31) / 32;           // token-SF TMEM columns per MMA
+  // NVFP4: token-SF columns of MMA k start every kTokSfStride columns (4-column aligned)
+  static constexpr int kTokSfStride = kTokSfCols <= 4 ? 4 : 8;
+  // NVFP4 with more than 128 tokens: two SF slots (2 x 192 accumulator columns + 2 x 64 = 512)
+  static constexpr int kSfSlots = (kBf16 || kF32) ? 1 : kFp4 ? (TOK > 128 ? 2 : 4)
+                                                             : (CPS == 1 && TOK <= 224 && WT == 1) ? 4 : 2;
   static_assert(kTokSfCols >= 1 && kTokSfCols <= 14, "token SF columns");
-  static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK <= 128 ? 64 : TOK <= 224 ? 56 : 224;   // token rows per TMA box
+  static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK <= 128 ? 64 : TOK == 192 ? 64 : TOK <= 224 ? 56 : 224;   // token rows per TMA box
   // Launched as a programmatic dependent of the preceding kernel (dispatch / route / quantise)
   // only for the small-batch tile: there the launch and prologue overlap that kernel's tail
   // (-0.9 us per graph-replayed decode step, -2 us eager).  The large-tile variants lost
@@ -130,8 +134,10 @@ struct Cfg {
   // starting every 8 columns (scale-factor TMEM addresses stay 4-column aligned)
   static constexpr int kSubSfCols = kSub / 32;
   static constexpr int kWSfCols = 4 * WT;
-  // NVFP4 slot: 16 weight-SF columns per weight tile (four MMAs x four), then 16 token-SF columns
-  static constexpr int kSfCols = (kBf16 || kF32) ? 0 : kFp4 ? 16 * WT + 16 : TOK <= 64 ? 8 : TOK <= 224 ? 16 : 32;
+  // NVFP4 slot: 16 weight-SF columns per weight tile (four MMAs x four), then four MMAs' token-SF
+  // columns kTokSfStride apart
+  static constexpr int kSfCols = (kBf16 || kF32) ? 0 : kFp4 ? 16 * WT + 4 * kTokSfStride
+                                                          : TOK <= 64 ? 8 : TOK <= 224 ? 16 : 32;
   static __device__ __forceinline__ int tok_sf_col(int c) {
     return kWSfCols + (c / kSubSfCols) * 8 + c % kSubSfCols;
   }
@@ -164,8 +170,8 @@ struct Cfg {
   static_assert(kSfBase + kSfSlots * kSfCols <= 512, "TMEM columns");
   static_assert(kBf16 || kF32 || kWSfCols + (TOK / kSub - 1) * 8 + kSubSfCols <= kSfCols, "SF slot width");
   static_assert(WT == 1 || (WT == 2 && CPS == 1 && (((FMT == kFmtFp8 || FMT == kFmtBf16) && TOK == 224) ||
-                                                    (FMT == kFmtNvfp4 && TOK == 128))),
-                "two weight tiles per item, one CTA per SM: FP8 or BF16 with 224 tokens, NVFP4 with 128");
+                                                    (FMT == kFmtNvfp4 && (TOK == 128 || TOK == 192)))),
+                "two weight tiles per item, one CTA per SM: FP8 or BF16 with 224 tokens, NVFP4 with 128 or 192");
   static_assert(!kF32 || ((TOK == 64 || TOK == 128) && CPS == 1) || (TOK == 32 && CPS == 2),
                 "FP32-scale tile: 64 or 128 tokens with one CTA per SM, or 32 with two (at most 64 FP32 "
                 "accumulators per thread)");
@@ -177,7 +183,8 @@ struct Cfg {
   static_assert(TOK % kBoxRows == 0, "whole TMA boxes must fit the token stage");
   static_assert(kSub % 32 == 0 && (kSub * kBlockK) % 1024 == 0, "sub-tile alignment");
   static_assert((kBoxRows * kBlockK) % 1024 == 0, "TMA boxes must keep the 1024-byte swizzle alignment");
-  static_assert(!kFp4 || (TOK <= 128 && MAXE <= kNvfp4MaxE), "NVFP4 tiles: at most 128 tokens, 256 experts");
+  static_assert(!kFp4 || ((TOK <= 128 || (TOK == 192 && WT == 2)) && MAXE <= kNvfp4MaxE),
+                "NVFP4 tiles: at most 128 tokens (192 in 256-row items), 256 experts");
 };
 
 struct Tile {
@@ -450,7 +457,7 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
           const uint64_t bdesc = smem_desc_k_sw128(smem_u32(stage_a + stage * C::kStageA));
           if constexpr (C::kFp4) {
             // four K = 64 steps; step k's scales: weight words at columns 4k, token words at 16 + 4k
-            // (NVFP4 tiles hold at most 128 tokens: one sub-tile, MMA N = mma_n <= 128)
+            // (NVFP4 tiles hold at most 192 tokens: one sub-tile, MMA N = mma_n <= 192)
             static_assert(!C::kFp4 || TOK == C::kSub, "NVFP4: one MMA sub-tile");
             // (two weight tiles: tile w's words at 16 w + 4k, token words at 16 WT + 4k)
             const uint32_t idesc = idesc_nvf4(kBlockW, mma_n);
@@ -463,7 +470,7 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
 #pragma unroll
               for (int w = 0; w < WT; ++w)
                 mma_nvf4(d_tmem + w * TOK, adw[w] + 2 * k, bdesc + 2 * k, idesc, sfw + 16 * w + 4 * k,
-                         sfw + 16 * WT + 4 * k, (kb | k) != 0);
+                         sfw + 16 * WT + C::kTokSfStride * k, (kb | k) != 0);
             }
           } else {
           // sub-tiles of at most kSub tokens: columns j*kSub.., smem rows j*kSub.., token SF columns j*kSub/32..
@@ -677,8 +684,8 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
       // no scale factors in tensor memory
     } else if constexpr (C::kFp4) {
       // NVFP4: the stage's scale words arrive with its data (TMA into shared memory); per stage,
-      // MMA k's word of weight row (lane + 32c) -> TMEM column 4k + c, of token row (lane + 32c)
-      // -> column 16 + 4k + c (rows past the tile: scale 0).  The shared-memory stage is released
+      // MMA k's word of weight row (lane + 32c) of weight tile w -> TMEM column 16w + 4k + c, of token
+      // row (lane + 32c) -> column 16 WT + kTokSfStride k + c (rows past the tile: scale 0).  The shared-memory stage is released
       // (one of the five arrivals on its empty barrier) as soon as the words are in registers.
       uint32_t stage = 0, phase = 0;
       for (int t = t_first; t < total_tiles && ok; t += G) {
@@ -719,7 +726,7 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
 #pragma unroll
-            for (int c = 0; c < C::kTokSfCols; ++c) tmem_st_x1(col + 16 * WT + 4 * k + c, a[k][c]);
+            for (int c = 0; c < C::kTokSfCols; ++c) tmem_st_x1(col + 16 * WT + C::kTokSfStride * k + c, a[k][c]);
           }
           tmem_wait_st();
           tc_fence_before();
@@ -983,9 +990,9 @@ extern "C" bsf_status bsf_grouped_gemm_nvfp4_contig(const uint8_t* a, const int3
   GemmArgs args{seg_start, counts, 0, m_cap, sfa, sfa_ld, sfb, static_cast<uint16_t*>(d),
                 static_cast<int>(E), static_cast<int>(N), static_cast<int>(K), err,
                 flags, a_exp, b_exp};
-  if (N % 256 == 0) {   // 256 x 128 items (two weight tiles), one CTA per SM
-    const int64_t max_items = (m_cap / 128 + E) * (N / 256);
-    return launch<128, 1, kNvfp4MaxE, kFmtNvfp4, 2>(args, a, b, max_items, reinterpret_cast<cudaStream_t>(stream));
+  if (N % 256 == 0) {   // 256 x 192 items (two weight tiles), one CTA per SM
+    const int64_t max_items = (m_cap / 192 + E) * (N / 256);
+    return launch<192, 1, kNvfp4MaxE, kFmtNvfp4, 2>(args, a, b, max_items, reinterpret_cast<cudaStream_t>(stream));
   }
   const int64_t max_tiles = (m_cap / 128 + E) * (N / 128);
   return launch<128, 2, kNvfp4MaxE, kFmtNvfp4>(args, a, b, max_tiles, reinterpret_cast<cudaStream_t>(stream));
@@ -1015,8 +1022,8 @@ extern "C" bsf_status bsf_grouped_gemm_nvfp4_masked(const uint8_t* a, const int3
     return launch<64, 2, kNvfp4MaxE, kFmtNvfp4>(args, a, b, max_tiles, s);
   }
   if (N % 256 == 0) {
-    const int64_t max_items = E * ((max_m + 127) / 128) * (N / 256);
-    return launch<128, 1, kNvfp4MaxE, kFmtNvfp4, 2>(args, a, b, max_items, s);
+    const int64_t max_items = E * ((max_m + 191) / 192) * (N / 256);
+    return launch<192, 1, kNvfp4MaxE, kFmtNvfp4, 2>(args, a, b, max_items, s);
   }
   const int64_t max_tiles = E * ((max_m + 127) / 128) * (N / 128);
   return launch<128, 2, kNvfp4MaxE, kFmtNvfp4>(args, a, b, max_tiles, s);
