@@ -25,7 +25,24 @@ DEVERR_SEGMENT = 0x10
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device pointer of a CUDA tensor; a host tensor here would be read or written by a kernel
+    through an address it cannot use, so it is refused before any library call."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _wptr(t, flags):
+    """Weights / weight scales: CUDA tensors, or pinned host tensors with B_HOST_MAPPED."""
+    if t is None:
+        return None
+    if flags & B_HOST_MAPPED:
+        if t.is_cuda or not t.is_pinned():
+            raise ValueError("B_HOST_MAPPED weights must be pinned host tensors (tensor.pin_memory())")
+        return ctypes.c_void_p(t.data_ptr())
+    return _ptr(t)
 
 
 def _stream(stream=None):
@@ -192,7 +209,7 @@ def grouped_gemm_contig(a, sfa, b, sfb, seg_start, counts, d=None, flags=0, stre
     if d is None:
         d = torch.empty((m_cap, N), dtype=torch.bfloat16, device=a.device)
     _lib.check(_lib.load().bsf_grouped_gemm_contig(
-        _ptr(a), _ptr(sfa), sfa.shape[1], m_cap, _ptr(b), _ptr(sfb), _ptr(d), _ptr(seg_start), _ptr(counts),
+        _ptr(a), _ptr(sfa), sfa.shape[1], m_cap, _wptr(b, flags), _wptr(sfb, flags), _ptr(d), _ptr(seg_start), _ptr(counts),
         E, N, K, flags, _stream(stream)), "grouped_gemm_contig")
     return d
 
@@ -204,7 +221,7 @@ def grouped_gemm_masked(a, sfa, b, sfb, masked_m, max_m, d=None, expected_m=0, f
     if d is None:
         d = torch.empty((E * max_m, N), dtype=torch.bfloat16, device=a.device)
     _lib.check(_lib.load().bsf_grouped_gemm_masked(
-        _ptr(a), _ptr(sfa), sfa.shape[1], _ptr(b), _ptr(sfb), _ptr(d), _ptr(masked_m), E, max_m, N, K,
+        _ptr(a), _ptr(sfa), sfa.shape[1], _wptr(b, flags), _wptr(sfb, flags), _ptr(d), _ptr(masked_m), E, max_m, N, K,
         expected_m, flags, _stream(stream)), "grouped_gemm_masked")
     return d
 
@@ -226,7 +243,8 @@ def checksum_u64(t, host_mapped=False, out=None, stream=None):
     nbytes = t.numel() * t.element_size()
     if out is None:
         out = torch.empty(1, dtype=torch.int64, device="cuda")
-    _lib.check(_lib.load().bsf_checksum_u64(_ptr(t), nbytes, B_HOST_MAPPED if host_mapped else 0, _ptr(out),
+    _lib.check(_lib.load().bsf_checksum_u64(_wptr(t, B_HOST_MAPPED if host_mapped else 0), nbytes,
+                                            B_HOST_MAPPED if host_mapped else 0, _ptr(out),
                                             _stream(stream)), "checksum_u64")
     return out
 
@@ -289,7 +307,7 @@ def grouped_gemm_nvfp4_contig(a, sfa, a_exp, b, sfb, b_exp, seg_start, counts, d
     if d is None:
         d = torch.empty((m_cap, N), dtype=torch.bfloat16, device=a.device)
     _lib.check(_lib.load().bsf_grouped_gemm_nvfp4_contig(
-        _ptr(a), _ptr(sfa), sfa.shape[1], m_cap, int(a_exp), _ptr(b), _ptr(sfb), _ptr(b_exp), _ptr(d),
+        _ptr(a), _ptr(sfa), sfa.shape[1], m_cap, int(a_exp), _wptr(b, flags), _wptr(sfb, flags), _ptr(b_exp), _ptr(d),
         _ptr(seg_start), _ptr(counts), E, N, 2 * K2, flags, _stream(stream)), "grouped_gemm_nvfp4_contig")
     return d
 
@@ -302,7 +320,7 @@ def grouped_gemm_nvfp4_masked(a, sfa, a_exp, b, sfb, b_exp, masked_m, max_m, d=N
     if d is None:
         d = torch.empty((E * max_m, N), dtype=torch.bfloat16, device=a.device)
     _lib.check(_lib.load().bsf_grouped_gemm_nvfp4_masked(
-        _ptr(a), _ptr(sfa), sfa.shape[1], int(a_exp), _ptr(b), _ptr(sfb), _ptr(b_exp), _ptr(d), _ptr(masked_m),
+        _ptr(a), _ptr(sfa), sfa.shape[1], int(a_exp), _wptr(b, flags), _wptr(sfb, flags), _ptr(b_exp), _ptr(d), _ptr(masked_m),
         E, max_m, N, 2 * K2, expected_m, flags, _stream(stream)), "grouped_gemm_nvfp4_masked")
     return d
 
@@ -315,7 +333,7 @@ def grouped_gemm_bf16_contig(a, b, seg_start, counts, d=None, flags=0, stream=No
     if d is None:
         d = torch.empty((m_cap, N), dtype=torch.bfloat16, device=a.device)
     _lib.check(_lib.load().bsf_grouped_gemm_bf16_contig(
-        _ptr(a), m_cap, _ptr(b), _ptr(d), _ptr(seg_start), _ptr(counts), E, N, K, flags, _stream(stream)),
+        _ptr(a), m_cap, _wptr(b, flags), _ptr(d), _ptr(seg_start), _ptr(counts), E, N, K, flags, _stream(stream)),
         "grouped_gemm_bf16_contig")
     return d
 
@@ -327,7 +345,7 @@ def grouped_gemm_bf16_masked(a, b, masked_m, max_m, d=None, expected_m=0, flags=
     if d is None:
         d = torch.empty((E * max_m, N), dtype=torch.bfloat16, device=a.device)
     _lib.check(_lib.load().bsf_grouped_gemm_bf16_masked(
-        _ptr(a), _ptr(b), _ptr(d), _ptr(masked_m), E, max_m, N, K, expected_m, flags, _stream(stream)),
+        _ptr(a), _wptr(b, flags), _ptr(d), _ptr(masked_m), E, max_m, N, K, expected_m, flags, _stream(stream)),
         "grouped_gemm_bf16_masked")
     return d
 
@@ -362,7 +380,7 @@ def grouped_gemm_f32sf_contig(a, sfa, b, sfb, seg_start, counts, d=None, flags=0
     if d is None:
         d = torch.empty((m_cap, N), dtype=torch.bfloat16, device=a.device)
     _lib.check(_lib.load().bsf_grouped_gemm_f32sf_contig(
-        _ptr(a), _ptr(sfa), sfa.shape[1], m_cap, _ptr(b), _ptr(sfb), _ptr(d), _ptr(seg_start), _ptr(counts),
+        _ptr(a), _ptr(sfa), sfa.shape[1], m_cap, _wptr(b, flags), _wptr(sfb, flags), _ptr(d), _ptr(seg_start), _ptr(counts),
         E, N, K, flags, _stream(stream)), "grouped_gemm_f32sf_contig")
     return d
 
@@ -374,6 +392,6 @@ def grouped_gemm_f32sf_masked(a, sfa, b, sfb, masked_m, max_m, d=None, expected_
     if d is None:
         d = torch.empty((E * max_m, N), dtype=torch.bfloat16, device=a.device)
     _lib.check(_lib.load().bsf_grouped_gemm_f32sf_masked(
-        _ptr(a), _ptr(sfa), sfa.shape[1], _ptr(b), _ptr(sfb), _ptr(d), _ptr(masked_m), E, max_m, N, K, expected_m,
+        _ptr(a), _ptr(sfa), sfa.shape[1], _wptr(b, flags), _wptr(sfb, flags), _ptr(d), _ptr(masked_m), E, max_m, N, K, expected_m,
         flags, _stream(stream)), "grouped_gemm_f32sf_masked")
     return d
