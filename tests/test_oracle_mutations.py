@@ -163,3 +163,53 @@ def test_f32sf_dropped_weight_scale_is_caught(monkeypatch):
     monkeypatch.setattr(f32sf, "grouped_gemm",
                         lambda aq, as_, bq, bs, seg, counts: orig(aq, as_, bq, np.ones_like(bs), seg, counts))
     _fails(pin_f32sf.test_gemm_exact_rational_brute_force)
+
+
+# ---------------------------------------------------------------- routing, packing, block shape
+def test_ignored_segment_alignment_is_caught(monkeypatch, golden_dir):
+    orig = route.route
+
+    def unaligned(topk_ids, num_experts, layout=route.CONTIGUOUS, align=1, max_m=0):
+        return orig(topk_ids, num_experts, layout, 1, max_m)              # align dropped
+
+    monkeypatch.setattr(route, "route", unaligned)
+    import json
+    import os
+    with open(os.path.join(golden_dir, "routing_example_t5_kr2_e4.json")) as f:
+        ex = json.load(f)
+    _fails(pin_route.test_worked_example_aligned_128, ex)
+
+
+def test_dropped_routes_counted_as_expert_zero_are_caught(monkeypatch):
+    orig = route.route
+
+    def drops_to_zero(topk_ids, num_experts, layout=route.CONTIGUOUS, align=1, max_m=0):
+        ids = np.asarray(topk_ids).copy()
+        ids[ids < 0] = 0                                                   # -1 routed to expert 0
+        return orig(ids, num_experts, layout, align, max_m)
+
+    monkeypatch.setattr(route, "route", drops_to_zero)
+    _fails(pin_route.test_brute_force_small, 0)
+
+
+def test_reversed_sf_byte_order_is_caught(monkeypatch):
+    orig = quantise.pack_sf
+
+    def big_endian(sf_bytes, ld=None):
+        w = orig(sf_bytes, ld).view(np.uint32)
+        return w.byteswap().view(np.int32)                                 # byte j <-> byte 3 - j
+
+    monkeypatch.setattr(quantise, "pack_sf", big_endian)
+    _fails(pin_quantise.test_pack_sf_byte_order_and_round_trip)
+
+
+def test_weight_blocks_of_1x128_are_caught(monkeypatch):
+    def rowwise(w_bf16_bits):
+        w = np.asarray(w_bf16_bits)
+        E, N, K = w.shape
+        q, by = quantise.quantise_act(w.reshape(E * N, K))                # 1 x 128 blocks instead of 128 x 128
+        s = np.ldexp(1.0, by.reshape(E, N, K // 128).astype(np.int64) - 127).astype(np.float32)
+        return q.reshape(E, N, K), s[:, ::128, :]
+
+    monkeypatch.setattr(quantise, "quantise_weight", rowwise)
+    _fails(pin_quantise.test_weight_blocks_are_128x128)
