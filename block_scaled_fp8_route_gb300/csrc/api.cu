@@ -7,27 +7,29 @@ namespace bsf {
 __device__ int g_device_error = 0;
 
 int* device_error_ptr() {
-  static int* cached[64] = {nullptr};
+  static std::atomic<int*> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (cached[dev] == nullptr) {
+  int* ptr = cached[dev].load(std::memory_order_acquire);
+  if (ptr == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    cached[dev] = static_cast<int*>(p);
+    ptr = static_cast<int*>(p);
+    cached[dev].store(ptr, std::memory_order_release);
   }
-  return cached[dev];
+  return ptr;
 }
 
 int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 }  // namespace bsf

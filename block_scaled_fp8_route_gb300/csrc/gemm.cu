@@ -842,10 +842,10 @@ bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int6
     if (!make_map_i32(&map_sfb, args.sfb, static_cast<int64_t>(args.E) * nw, args.N, kBlockW, 4)) return BSF_ERR_CUDA;
     if (!make_map_i32(&map_sfa, args.sfa, nw, args.sfa_ld, C::kSfTokCols, 4)) return BSF_ERR_CUDA;
   }
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];   // setting the attributes twice (racing first calls) is harmless
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(grouped_gemm_kernel<TOK, CPS, MAXE, FMT, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::kSmem)) != cudaSuccess)
       return BSF_ERR_CUDA;
@@ -853,7 +853,7 @@ bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int6
                                         cudaFuncAttributePreferredSharedMemoryCarveout,
                                         cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return BSF_ERR_CUDA;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   int64_t grid = static_cast<int64_t>(sm_count()) * CPS;
   if (max_tiles < grid) grid = max_tiles;

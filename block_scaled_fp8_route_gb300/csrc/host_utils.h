@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/bsfroute.h"
 
 namespace bsf {
@@ -44,6 +46,11 @@ inline bsf_status launch_dependent(void (*kernel)(Params...), unsigned grid, uns
   }
   return launch_status();
 }
+
+// Per-device values the library resolves on first use are cached in atomics, so
+// first calls from several host threads at once are well defined (each stores
+// the same value).  The caches are not invalidated: after cudaDeviceReset() the
+// process must not call the library again on that device.
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

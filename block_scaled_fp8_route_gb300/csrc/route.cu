@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kThreads) route_fill_kernel(int E, int64_t m_c
 using namespace bsf;
 
 extern "C" size_t bsf_route_workspace_bytes(int64_t T, int64_t kr, int64_t E) {
-  if (T < 0 || kr <= 0 || E <= 0) return 0;
+  if (T < 0 || kr <= 0 || E <= 0 || T > INT32_MAX / kr) return 0;   // T * kr is formed only when it fits
   const int64_t R = T * kr;
   const int64_t nblk = (R + kChunk - 1) / kChunk;
   return static_cast<size_t>((nblk > 0 ? nblk : 1) * E * sizeof(int32_t));
@@ -294,12 +294,12 @@ bsf_status route_impl(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E,
                       void* workspace, size_t workspace_bytes, bsf_stream_t stream) {
   if (T < 0 || kr <= 0 || E <= 0 || E > kMaxExperts) return BSF_ERR_INVALID_ARGUMENT;
   if (layout != BSF_LAYOUT_CONTIGUOUS && layout != BSF_LAYOUT_MASKED) return BSF_ERR_INVALID_ARGUMENT;
-  if (align_or_max_m < 1) return BSF_ERR_INVALID_ARGUMENT;
+  if (align_or_max_m < 1 || align_or_max_m > INT32_MAX) return BSF_ERR_INVALID_ARGUMENT;
   if (!counts || !seg_start || !output_index || !token_of_row) return BSF_ERR_INVALID_ARGUMENT;
+  if (T > INT32_MAX / kr) return BSF_ERR_UNSUPPORTED;   // before forming R, which must not wrap
   const int64_t R = T * kr;
   const int64_t need_cap = layout == BSF_LAYOUT_MASKED ? E * align_or_max_m : R + E * (align_or_max_m - 1);
   if (m_cap < need_cap || m_cap > INT32_MAX) return BSF_ERR_INVALID_ARGUMENT;
-  if (R > INT32_MAX) return BSF_ERR_UNSUPPORTED;
   if (workspace_bytes < bsf_route_workspace_bytes(T, kr, E) || !workspace) return BSF_ERR_INVALID_ARGUMENT;
   if (q && fmt == kRowsBf16) {
     if (!a_packed || K <= 0 || K % 8) return BSF_ERR_INVALID_ARGUMENT;
@@ -390,11 +390,12 @@ extern "C" bsf_status bsf_route_bf16(const int32_t* topk_ids, int64_t T, int64_t
 // ---------------------------------------------------------------------------
 // Allocation-free variant of bsf_route.
 //
-// For callers that cannot allocate device memory themselves: code running
-// while a CUDA graph is being captured (allocation is not a capturable
-// operation), code inside an allocator-free runtime, or hosts that must not
-// grow device memory after start-up.  The per-chunk expert counts live in a
-// fixed file-scope device array instead of a caller-provided workspace.
+// For callers that cannot call cudaMalloc where they route: serving runtimes
+// that reserve all device memory at start-up (an allocation would fail or
+// fragment their pool, and cudaMalloc synchronises the device), plug-ins whose
+// host framework owns the allocator, and code inside an allocator callback.
+// The per-chunk expert counts live in a fixed file-scope device array instead
+// of a caller-provided workspace.
 namespace bsf {
 namespace {
 
@@ -405,23 +406,25 @@ static __device__ __align__(256) int32_t g_route_scratch[kRouteStaticScratchByte
 
 // Device address of g_route_scratch for the current device, resolved once per
 // device with that device current (the host-side name is only a stand-in).
+// The cache entries are atomics: first calls from several host threads may
+// race to fill an entry, and each stores the same address.
 int32_t* route_scratch_ptr(bsf_status* st) {
-  static int32_t* cached[64] = {nullptr};
+  static std::atomic<int32_t*> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     *st = BSF_ERR_CUDA;
     return nullptr;
   }
-  if (cached[dev] == nullptr) {
-    int32_t* ptr = nullptr;
+  int32_t* ptr = cached[dev].load(std::memory_order_acquire);
+  if (ptr == nullptr) {
     if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_route_scratch) != cudaSuccess || ptr == nullptr) {
       *st = BSF_ERR_CUDA;
       return nullptr;
     }
-    cached[dev] = ptr;
+    cached[dev].store(ptr, std::memory_order_release);
   }
   *st = BSF_OK;
-  return cached[dev];
+  return ptr;
 }
 
 }  // namespace
@@ -434,6 +437,7 @@ extern "C" bsf_status bsf_route_no_alloc(const int32_t* topk_ids, int64_t T, int
                                          int64_t K, uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld,
                                          bsf_stream_t stream) {
   if (T < 0 || kr <= 0 || E <= 0) return BSF_ERR_INVALID_ARGUMENT;
+  if (T > INT32_MAX / kr) return BSF_ERR_UNSUPPORTED;
   const size_t need = bsf_route_workspace_bytes(T, kr, E);
   if (need > kRouteStaticScratchBytes) return BSF_ERR_UNSUPPORTED;   // problem larger than the static scratch
   bsf_status st = BSF_OK;

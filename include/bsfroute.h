@@ -159,7 +159,9 @@ bsf_status bsf_prepare_weight_sf(const float* sf128, int64_t E, int64_t N, int64
  *                 no GEMM output row that is stored depends on them).
  *   sfa_packed    int32 [ceil(K/512)][sfa_ld] (output), sfa_ld >= m_cap,
  *                 multiple of 4; padding rows are not written.
- *   workspace     device scratch of bsf_route_workspace_bytes(T, kr, E) bytes.
+ *   workspace     device scratch of bsf_route_workspace_bytes(T, kr, E) bytes
+ *                 (that function returns 0 for sizes bsf_route rejects:
+ *                 T < 0, kr <= 0, E <= 0, or T * kr above INT32_MAX).
  * Order inside an expert: ascending flat index t*kr + r (stable; the order of
  * the worked example in §4.3 / §4.6).  Deterministic.
  */
@@ -173,11 +175,15 @@ bsf_status bsf_route(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, 
 /*
  * bsf_route_no_alloc — bsf_route without a caller-provided workspace.
  * The pages have no counterpart of this entry point; it exists for callers
- * that cannot allocate device memory at the call site: work recorded while a
- * CUDA graph is being captured (allocation is not capturable), runtimes that
- * forbid allocation after start-up, or code without access to an allocator.
+ * that cannot call cudaMalloc where they route: serving runtimes that reserve
+ * all device memory at start-up and hand the library only its inputs and
+ * outputs (cudaMalloc would fail or fragment their pool, and it synchronises
+ * the device, stalling every other stream), plug-ins whose host framework owns
+ * the allocator and forbids direct device allocation, and code running inside
+ * an allocator callback or memory-pressure handler, where allocating again
+ * could re-enter the allocator.
  * Same arguments, outputs and errors as bsf_route minus workspace /
- * workspace_bytes.  The scratch is a file-scope device array of
+ * workspace_bytes (T * kr above INT32_MAX is BSF_ERR_UNSUPPORTED).  The scratch is a file-scope device array of
  * BSF_ROUTE_STATIC_SCRATCH_BYTES bytes (256 KiB) that every GPU which loads
  * the library holds until the process exits; a problem whose
  * bsf_route_workspace_bytes(T, kr, E) exceeds it is rejected with
@@ -231,6 +237,12 @@ bsf_status bsf_dispatch(const void* x, int64_t T, int64_t K, const int32_t* topk
  * device-resident weights) is launched as a programmatic dependent
  * of the preceding kernel on the stream: its CTAs may be scheduled while that
  * kernel drains, and they touch no global memory until it has completed.
+ *
+ * Tensor memory: every GEMM CTA allocates its tensor-memory columns on entry
+ * (tcgen05.alloc), which waits, with no time limit, until an SM has that many
+ * columns free.  GEMMs enqueued on two streams of one device can share an SM;
+ * a CTA of the second then waits until a CTA of the first exits.  Both finish
+ * (every other wait in the kernels is bounded), but they serialise on the SM.
  *
  * bsf_grouped_gemm_contig — D[r, :] = BF16( dequant(A[r, :]) . dequant(B_e)^T )
  * for every expert e and every row r in [seg_start[e], seg_start[e] + counts[e]).

@@ -29,6 +29,9 @@ def test_host_only_calls(lib):
     # workspace size is host arithmetic: one int32 per (2048-assignment chunk, expert)
     assert lib.bsf_route_workspace_bytes(8192, 8, 256) == 32 * 256 * 4
     assert lib.bsf_route_workspace_bytes(1, 1, 4) == 16
+    # T * kr above INT32_MAX: refused (0 bytes) without forming the product
+    assert lib.bsf_route_workspace_bytes(2**31, 8, 8) == 0
+    assert lib.bsf_route_workspace_bytes(2**62, 4, 8) == 0
 
 
 def test_argument_validation_needs_no_device(lib):
@@ -40,6 +43,13 @@ def test_argument_validation_needs_no_device(lib):
     # unknown layout
     assert lib.bsf_route(nul, 4, 2, 4, 7, 1, nul, nul, nul, nul, nul, 8, nul, nul, 0, 0, nul, nul, 0, nul, 0,
                          nul) == 1
+    # T * kr above INT32_MAX (would wrap as a 64-bit product too at T = 2**62): unsupported, nothing enqueued
+    fake = ctypes.c_void_p(256)
+    for T, kr in ((2**31, 8), (2**62, 4)):
+        assert lib.bsf_route(nul, T, kr, 8, 0, 1, fake, fake, fake, fake, nul, 1 << 30, nul, nul, 0, 0, nul, nul, 0,
+                             fake, 1 << 20, nul) == 3
+        assert lib.bsf_route_no_alloc(nul, T, kr, 8, 0, 1, fake, fake, fake, fake, nul, 1 << 30, nul, nul, 0, 0, nul,
+                                      nul, 0, nul) == 3
     # combine with N not a multiple of 8
     assert lib.bsf_combine(nul, 4, nul, nul, 2, 2, 12, nul, nul) == 1
     # dispatch: batch above the single-launch limit is unsupported, K not a multiple of 128 invalid

@@ -1,12 +1,15 @@
 """bsf_route_no_alloc: routing without a caller-provided workspace.
 
-Some callers cannot allocate device memory where they call the router (while
-a CUDA graph is being captured, or inside a runtime that forbids allocation
-after start-up).  This entry point keeps its scratch in a fixed device array
-of the library.  Its outputs must equal those of bsf_route (with a
-caller-allocated workspace) bit for bit — routing is integer work — on two
-calls in a row, the second with different inputs so that the first call's
-leftover scratch contents are exercised.  Collected last on purpose.
+Some callers cannot call cudaMalloc where they route: serving runtimes that
+reserve all device memory at start-up, plug-ins whose host framework owns the
+allocator, code inside an allocator callback.  This entry point keeps its
+scratch in a fixed device array of the library.  Its outputs must equal those
+of bsf_route (with a caller-allocated workspace) bit for bit — routing is
+integer work — on two calls in a row, the second with different inputs so that
+the first call's leftover scratch contents are exercised.  Both workloads are
+large enough (T * k_r > 16384 assignments) to take the multi-block count /
+scan / assign path, the one that uses the scratch array.  Collected last on
+purpose.
 """
 
 import ctypes
@@ -56,7 +59,7 @@ def _compare(b_ref, b_new):
     assert torch.equal(b_ref["sfa_packed"][:, :used][:, routed], b_new["sfa_packed"][:, :used][:, routed])
 
 
-@pytest.mark.parametrize("name", ["large", "decode"])
+@pytest.mark.parametrize("name", ["large", "prefill"])
 def test_no_alloc_route_matches_workspace_route_twice(name):
     dev = require_gpu()
     lib = _lib.load()
@@ -69,6 +72,7 @@ def test_no_alloc_route_matches_workspace_route_twice(name):
         ids, _ = W.routing(wl, device=dev)
         x = W.activations(wl, device=dev, K=K)
         q, sf = ops.quantise_act(x)
+        assert w.T * w.kr > 16384              # above the single-CTA limit: count / scan / assign kernels
         ws = torch.empty(lib.bsf_route_workspace_bytes(w.T, w.kr, w.E), dtype=torch.uint8, device=dev)
         assert ws.numel() <= STATIC_SCRATCH_BYTES
         b_ref = _bufs(w.T, w.kr, w.E, w.layout, a_or_m, K, dev)
@@ -88,6 +92,18 @@ def test_no_alloc_route_rejects_oversize_problems():
     T, kr, E = 65536, 8, 1024          # 256 chunks x 1024 experts x 4 B = 1 MiB > 256 KiB
     assert lib.bsf_route_workspace_bytes(T, kr, E) > STATIC_SCRATCH_BYTES
     nul = ctypes.c_void_p(0)
+    st = lib.bsf_route_no_alloc(nul, T, kr, E, 0, 1, nul, nul, nul, nul, nul, T * kr, nul, nul, 0, 0, nul, nul,
+                                0, nul)
+    assert st == 3    # BSF_ERR_UNSUPPORTED, nothing enqueued
+
+
+def test_no_alloc_route_rejects_assignment_count_overflow():
+    """T * kr above INT32_MAX is refused before the product is formed."""
+    require_gpu()
+    lib = _lib.load()
+    nul = ctypes.c_void_p(0)
+    T, kr, E = 2**31, 8, 8
+    assert lib.bsf_route_workspace_bytes(T, kr, E) == 0
     st = lib.bsf_route_no_alloc(nul, T, kr, E, 0, 1, nul, nul, nul, nul, nul, T * kr, nul, nul, 0, 0, nul, nul,
                                 0, nul)
     assert st == 3    # BSF_ERR_UNSUPPORTED, nothing enqueued
