@@ -196,13 +196,13 @@ def test_decode_full_size_sampled(dev):
 
 
 def test_prefill_full_size_sampled(dev):
-    _workload_gemm_check(dev, "prefill", n_sample=3)
-    _workload_gemm_check(dev, "prefill", n_sample=2, second=True)
+    _workload_gemm_check(dev, "prefill", n_sample=6)
+    _workload_gemm_check(dev, "prefill", n_sample=6, second=True)
 
 
 def test_large_full_size_sampled(dev):
-    _workload_gemm_check(dev, "large", n_sample=2)
-    _workload_gemm_check(dev, "large", n_sample=1, second=True)
+    _workload_gemm_check(dev, "large", n_sample=6)
+    _workload_gemm_check(dev, "large", n_sample=6, second=True)
 
 
 def test_bitwise_determinism_20_runs(dev):
