@@ -64,3 +64,31 @@ def oracle_packed_operand(aq, asf_bytes, token_of_row):
     rows = oracle.route.scatter_rows(aq, token_of_row)
     sfb = oracle.route.scatter_rows(asf_bytes, token_of_row, pad_value=127)
     return rows, sfb
+
+
+def check_combine_of_own_y(z_gpu_bits, y_gpu_bits, output_index, topk_weights, what):
+    """The combine kernel alone: z from the GPU's own y against the float64 combine of that y.
+
+    The kernel accumulates k_r products in FP32 and rounds once to bf16, so
+    |z - z64| <= one bf16 step of z64 (2**-7 |z64|) + the FP32 summation error
+    2 k_r 2**-24 sum_r |p_r y_r| (the factor 2 covers the final rounding of a
+    sum that moved across a power of two).  Without cancellation the second
+    term is far below the first; where the k_r terms cancel it is what remains.
+    """
+    z_own = oracle.combine.combine(y_gpu_bits, output_index, topk_weights)
+    y = oracle.formats.bf16_bits_to_f64(y_gpu_bits)
+    idx = np.asarray(output_index)
+    p = np.abs(np.asarray(topk_weights, dtype=np.float32).astype(np.float64))
+    mag = np.zeros((idx.shape[0], y.shape[1]))
+    for r in range(idx.shape[1]):
+        ok = idx[:, r] >= 0
+        mag[ok] += p[ok, r:r + 1] * np.abs(y[idx[ok, r]])
+    zo = oracle.formats.bf16_bits_to_f64(z_own)
+    bound = np.abs(zo) * 2.0 ** -7 + 2.0 * idx.shape[1] * 2.0 ** -24 * mag + 1e-30
+    d = np.abs(oracle.formats.bf16_bits_to_f64(z_gpu_bits) - zo)
+    bad = d > bound
+    if bad.any():
+        t, n = np.unravel_index(np.argmax(d / bound), d.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} elements of the combine outside one bf16 step + FP32 "
+                             f"summation error, worst [{t}, {n}]: |d| {d[t, n]:.3e}, bound {bound[t, n]:.3e}, "
+                             f"z64 {zo[t, n]:.3e}, sum|p y| {mag[t, n]:.3e}")

@@ -8,7 +8,8 @@ import torch
 import oracle
 import workloads as W
 from block_scaled_fp8_route_gb300 import MoEPath, ops
-from tests.gpu_util import bits16, check_combined, check_expert_block, expert_row_rms, i32, require_gpu
+from tests.gpu_util import (bits16, check_combine_of_own_y, check_combined, check_expert_block, expert_row_rms, i32,
+                            require_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -67,11 +68,8 @@ def test_end_to_end(dev, name):
             check_expert_block(yg[s:s + c], y_ref[s:s + c], f"{name} expert {e}")
     rms = expert_row_rms(y_ref, r["seg_start"], r["counts"])
     check_combined(bits16(z), z_ref, y_ref, r["output_index"], p.numpy(), rms, f"{name} combined output")
-    # combine of the GPU's own y is within one bf16 step of the float64 combine of that y
-    z_from_gpu_y = oracle.combine.combine(yg, r["output_index"], p.numpy())
-    d = np.abs(oracle.formats.bf16_bits_to_f64(bits16(z)) - oracle.formats.bf16_bits_to_f64(z_from_gpu_y))
-    step = np.abs(oracle.formats.bf16_bits_to_f64(z_from_gpu_y)) * 2.0 ** -7 + 1e-30
-    assert np.all(d <= step)
+    # combine of the GPU's own y against the float64 combine of that y
+    check_combine_of_own_y(bits16(z), yg, r["output_index"], p.numpy(), f"{name} combine")
 
 
 def test_end_to_end_deterministic(dev):
