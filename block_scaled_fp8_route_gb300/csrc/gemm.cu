@@ -31,12 +31,12 @@
 //   512 K and the byte is picked with sf_id = k_block % 4;
 // * epilogue: tcgen05.ld 32 columns (tokens) per thread row (weight row),
 //   transposed through shared memory into 64-byte row segments of D.
-#include <cudaTypedefs.h>
-
 #include "common.cuh"
 #include "host_utils.h"
+#include "tma_map.h"
 
 namespace bsf {
+
 namespace {
 
 constexpr int kBlockW = 128;        // weight rows per tile (MMA M)
@@ -158,7 +158,12 @@ struct Cfg {
   static constexpr int kEpiWarps = 4 * kEpiGroups;
   // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue group 0, warps 6-9 SF loaders
   // (epilogue group 1 when kF32Wide), warps 10.. further epilogue groups
-  static constexpr int kNumThreads = kF32Wide ? 320 : 32 * (2 + kEpiWarps + 4);
+  // WT = 2: one more warp, the waiter, performs every mbarrier wait of the MMA issuer and hands each
+  // stage over through named barrier kHandoffBar, so the issuing thread reads no shared memory
+  static constexpr bool kWaiter = WT == 2;
+  static constexpr int kWaiterWarp = 2 + kEpiWarps + 4;
+  static constexpr int kHandoffBar = 1;
+  static constexpr int kNumThreads = kF32Wide ? 320 : 32 * (2 + kEpiWarps + 4 + (kWaiter ? 1 : 0));
   static constexpr int kEpiBytes = kEpiWarps * 32 * 32 * 2;   // per epilogue warp: 32 tokens x 32 columns bf16
   static constexpr int kTableBytes = (3 * MAXE + 4) * 4;
   static constexpr int kBarBytes = 512;
@@ -436,7 +441,107 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
       }
       tc_commit(mma_done);
       drain_wait(mma_done, 0);
-    } else if (!C::kF32 && lane == 0) {
+    } else if (!C::kF32) {
+      // One stage's MMAs (K = 128 bytes of both operands) into accumulator d_tmem, issued as
+      // straight-line code: a branch between two tcgen05.mma instructions stalls the tensor pipe.
+      auto issue_stage = [&](uint32_t stage, uint32_t sf_slot, uint32_t d_tmem, uint32_t mma_n, int kb) {
+        const uint32_t sfw = tmem_base + C::kSfBase + sf_slot * C::kSfCols;
+        const uint32_t sft = sfw + C::kWSfCols;
+        const uint64_t adesc = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB));
+        const uint64_t bdesc = smem_desc_k_sw128(smem_u32(stage_a + stage * C::kStageA));
+        if constexpr (C::kFp4) {
+          // four K = 64 steps; step k's scales: weight words at columns 4k, token words at 16 + 4k
+          // (NVFP4 tiles hold at most 192 tokens: one sub-tile, MMA N = mma_n <= 192)
+          static_assert(!C::kFp4 || TOK == C::kSub, "NVFP4: one MMA sub-tile");
+          // (two weight tiles: tile w's words at 16 w + 4k, token words at 16 WT + 4k)
+          const uint32_t idesc = idesc_nvf4(kBlockW, mma_n);
+          uint64_t adw[WT];
+#pragma unroll
+          for (int w = 0; w < WT; ++w)
+            adw[w] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + w * kBlockW * kBlockK));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+#pragma unroll
+            for (int w = 0; w < WT; ++w)
+              mma_nvf4(d_tmem + w * TOK, adw[w] + 2 * k, bdesc + 2 * k, idesc, sfw + 16 * w + 4 * k,
+                       sfw + 16 * WT + C::kTokSfStride * k, (kb | k) != 0);
+          }
+        } else {
+        // sub-tiles of at most kSub tokens: columns j*kSub.., smem rows j*kSub.., token SF columns j*kSub/32..
+#pragma unroll
+        for (int j = 0; j < TOK / C::kSub; ++j) {
+          const int n_j = static_cast<int>(mma_n) - j * C::kSub;
+          if (n_j <= 0) break;
+          const uint32_t nn = n_j < C::kSub ? n_j : C::kSub;    // MMA N of this sub-tile: 16..224
+          const uint64_t bd = bdesc + static_cast<uint64_t>(j * C::kSub * kBlockK >> 4);
+          if constexpr (C::kBf16) {
+            // four K = 16 steps of 32 bytes inside the swizzled 128-byte rows
+            const uint32_t idesc = idesc_bf16(kBlockW, nn);
+            uint64_t adw[WT];
+#pragma unroll
+            for (int w = 0; w < WT; ++w)
+              adw[w] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + w * kBlockW * kBlockK));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+#pragma unroll
+              for (int w = 0; w < WT; ++w)
+                mma_bf16(d_tmem + w * TOK + j * C::kSub, adw[w] + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+            }
+          } else {
+            const uint32_t idesc = idesc_mxf8_e4m3(kBlockW, nn, kb & 3, kb & 3);
+            uint64_t adw[WT];              // weight tile w of the stage; its accumulator block and SF columns
+#pragma unroll
+            for (int w = 0; w < WT; ++w)
+              adw[w] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + w * kBlockW * kBlockK));
+#pragma unroll
+            for (int k = 0; k < kBlockK / 32; ++k) {
+              // advance 32 bytes (one K=32 step of FP8) inside the swizzled 128-byte rows
+#pragma unroll
+              for (int w = 0; w < WT; ++w)
+                mma_mxf8(d_tmem + w * TOK + j * C::kSub, adw[w] + 2 * k, bd + 2 * k, idesc, sfw + 4 * w,
+                         sft + j * 8, (kb | k) != 0);
+            }
+          }
+        }
+        }
+      };
+      if constexpr (C::kWaiter) {
+        // The issuing thread reads no shared memory between stages: any load there (an mbarrier
+        // wait, even on a completed phase, or a plain flag) lets the tensor pipe drain before the
+        // next MMAs (measured: a 4-MMA stage of N = 128 grows from 256 to ~440 cycles).  The waiter
+        // warp does every wait and hands each stage over through named barrier kHandoffBar, whose
+        // OR-reduced predicate carries an abort.  The whole warp runs the loop; lane 0 issues.
+        uint32_t stage = 0, sf_slot = 0, acc = 0;
+        bool ok = true;
+        for (int t = t_first; t < total_tiles && ok; t += G) {
+          const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nit, TOK);
+          const uint32_t mma_n = (tl.ntok + 15) & ~15;
+          const uint32_t d_tmem = tmem_base + acc * C::kAccCols;
+          for (int kb = 0; kb < nkb; ++kb) {
+            // this stage's data (for kb = 0 also the drained accumulator; per slot the scales) is ready
+            if (named_barrier_or(C::kHandoffBar, 64, false)) { ok = false; break; }
+            if (lane == 0) {
+              tc_fence_after();
+              issue_stage(stage, sf_slot, d_tmem, mma_n, kb);
+              tc_commit(&empty[stage]);
+              if (!C::kBf16 && (kb % C::kKbPerSlot == C::kKbPerSlot - 1 || kb == nkb - 1)) tc_commit(&sf_empty[sf_slot]);
+            }
+            __syncwarp();
+            if (++stage == C::kStages) stage = 0;
+            if (!C::kBf16 && (kb % C::kKbPerSlot == C::kKbPerSlot - 1 || kb == nkb - 1))
+              if (++sf_slot == C::kSfSlots) sf_slot = 0;
+          }
+          if (!ok) break;
+          if (lane == 0) tc_commit(&acc_full[acc]);
+          __syncwarp();
+          if (++acc == C::kAccBufs) acc = 0;
+        }
+        // wait for every MMA issued by this thread before TMEM can be released
+        if (lane == 0) {
+          tc_commit(mma_done);
+          drain_wait(mma_done, 0);
+        }
+      } else if (lane == 0) {
       uint32_t stage = 0, phase = 0, sf_slot = 0, sf_phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int t = t_first; t < total_tiles && ok; t += G) {
@@ -451,65 +556,7 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
           }
           if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sfw = tmem_base + C::kSfBase + sf_slot * C::kSfCols;
-          const uint32_t sft = sfw + C::kWSfCols;
-          const uint64_t adesc = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB));
-          const uint64_t bdesc = smem_desc_k_sw128(smem_u32(stage_a + stage * C::kStageA));
-          if constexpr (C::kFp4) {
-            // four K = 64 steps; step k's scales: weight words at columns 4k, token words at 16 + 4k
-            // (NVFP4 tiles hold at most 192 tokens: one sub-tile, MMA N = mma_n <= 192)
-            static_assert(!C::kFp4 || TOK == C::kSub, "NVFP4: one MMA sub-tile");
-            // (two weight tiles: tile w's words at 16 w + 4k, token words at 16 WT + 4k)
-            const uint32_t idesc = idesc_nvf4(kBlockW, mma_n);
-            uint64_t adw[WT];
-#pragma unroll
-            for (int w = 0; w < WT; ++w)
-              adw[w] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + w * kBlockW * kBlockK));
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-#pragma unroll
-              for (int w = 0; w < WT; ++w)
-                mma_nvf4(d_tmem + w * TOK, adw[w] + 2 * k, bdesc + 2 * k, idesc, sfw + 16 * w + 4 * k,
-                         sfw + 16 * WT + C::kTokSfStride * k, (kb | k) != 0);
-            }
-          } else {
-          // sub-tiles of at most kSub tokens: columns j*kSub.., smem rows j*kSub.., token SF columns j*kSub/32..
-#pragma unroll
-          for (int j = 0; j < TOK / C::kSub; ++j) {
-            const int n_j = static_cast<int>(mma_n) - j * C::kSub;
-            if (n_j <= 0) break;
-            const uint32_t nn = n_j < C::kSub ? n_j : C::kSub;    // MMA N of this sub-tile: 16..224
-            const uint64_t bd = bdesc + static_cast<uint64_t>(j * C::kSub * kBlockK >> 4);
-            if constexpr (C::kBf16) {
-              // four K = 16 steps of 32 bytes inside the swizzled 128-byte rows
-              const uint32_t idesc = idesc_bf16(kBlockW, nn);
-              uint64_t adw[WT];
-#pragma unroll
-              for (int w = 0; w < WT; ++w)
-                adw[w] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + w * kBlockW * kBlockK));
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-#pragma unroll
-                for (int w = 0; w < WT; ++w)
-                  mma_bf16(d_tmem + w * TOK + j * C::kSub, adw[w] + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
-              }
-            } else {
-              const uint32_t idesc = idesc_mxf8_e4m3(kBlockW, nn, kb & 3, kb & 3);
-              uint64_t adw[WT];              // weight tile w of the stage; its accumulator block and SF columns
-#pragma unroll
-              for (int w = 0; w < WT; ++w)
-                adw[w] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + w * kBlockW * kBlockK));
-#pragma unroll
-              for (int k = 0; k < kBlockK / 32; ++k) {
-                // advance 32 bytes (one K=32 step of FP8) inside the swizzled 128-byte rows
-#pragma unroll
-                for (int w = 0; w < WT; ++w)
-                  mma_mxf8(d_tmem + w * TOK + j * C::kSub, adw[w] + 2 * k, bd + 2 * k, idesc, sfw + 4 * w,
-                           sft + j * 8, (kb | k) != 0);
-              }
-            }
-          }
-          }
+          issue_stage(stage, sf_slot, d_tmem, mma_n, kb);
           tc_commit(&empty[stage]);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
           if (!C::kBf16 && (kb % C::kKbPerSlot == C::kKbPerSlot - 1 || kb == nkb - 1)) {
@@ -524,9 +571,28 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
       // wait for every MMA issued by this thread before TMEM can be released
       tc_commit(mma_done);
       drain_wait(mma_done, 0);
+      }
     }
     __syncwarp();
-  } else if (warp < 6 || warp >= 10 || (C::kF32Wide && warp < 10)) {
+  } else if (C::kWaiter && warp == C::kWaiterWarp) {
+    // ------------------------------------------------------------ waiter (two-weight-tile items)
+    // Every wait of the MMA issuer, in the issuer's order; each stage is handed over through the
+    // named barrier (the OR of its predicate tells the issuer to stop).
+    uint32_t stage = 0, phase = 0, sf_slot = 0, sf_phase = 0, acc = 0, acc_phase = 0;
+    bool ok = true;
+    for (int t = t_first; t < total_tiles && ok; t += G) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        bool good = kb != 0 || warp_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.err);
+        if (good && !C::kBf16 && kb % C::kKbPerSlot == 0) good = warp_wait(&sf_full[sf_slot], sf_phase, abort_flag, p.err);
+        if (good) good = warp_wait(&full[stage], phase, abort_flag, p.err);
+        if (named_barrier_or(C::kHandoffBar, 64, !good)) { ok = false; break; }
+        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        if (!C::kBf16 && (kb % C::kKbPerSlot == C::kKbPerSlot - 1 || kb == nkb - 1))
+          if (++sf_slot == C::kSfSlots) { sf_slot = 0; sf_phase ^= 1u; }
+      }
+      if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
+    }
+  } else if (warp < 6 || (warp >= 10 && warp < 10 + 4 * (C::kEpiGroups - 1)) || (C::kF32Wide && warp < 10)) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // TMEM lane quadrant = weight rows 32q..32q+31
     const int ew = warp < 10 ? warp - 2 : warp - 6;  // epilogue warp 0 .. kEpiWarps-1
@@ -781,47 +847,6 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// 2-D uint8 tensor [rows, cols] (row pitch = cols bytes), box {128 cols, box_rows}, 128-byte swizzle.
-// 2-D int32 tensor [rows, cols] (row pitch = cols words), box {box_cols, box_rows}, no swizzle;
-// reads past the edges fill zeros.  Scale words of the NVFP4 stages.
-bool make_map_i32(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, uint32_t box_cols,
-                  uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t estr[2] = {1u, 1u};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
-  const cuuint32_t box[2] = {128u, box_rows};
-  const cuuint32_t estr[2] = {1u, 1u};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int TOK, int CPS = 1, int MAXE = kMaxExperts, int FMT = kFmtFp8, int WT = 1>
 bsf_status launch(const GemmArgs& args, const uint8_t* a, const uint8_t* b, int64_t max_tiles, cudaStream_t s) {
   using C = Cfg<TOK, CPS, MAXE, FMT, WT>;
