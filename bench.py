@@ -134,7 +134,9 @@ def step_work(w, counts, placed_rows, fused_dispatch=False, fmt="fp8"):
     out_n = N
     if w.K2:
         qb2, sb2 = operand_bytes(w.K2, fmt)
-        if fmt != "bf16":
+        if fmt == "fp8":   # only the routed rows of the packed input are quantised
+            b["quantise2"] = rows * w.K2 * 2 + rows * (qb2 + sb2)
+        elif fmt != "bf16":
             b["quantise2"] = placed_rows * w.K2 * 2 + placed_rows * (qb2 + sb2)
         b["gemm2"] = len(active) * weight_bytes(w.N2, w.K2, fmt) + rows * (qb2 + sb2 + w.N2 * 2)
         flops += 2.0 * rows * w.N2 * w.K2
@@ -145,8 +147,9 @@ def step_work(w, counts, placed_rows, fused_dispatch=False, fmt="fp8"):
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """SM clock and throttle reasons sampled every ~2 ms through NVML (ctypes on the
-    driver's libnvidia-ml) while the timed region runs; nvidia-smi as a fallback."""
+    """SM clock and throttle reasons sampled every ~0.2 ms through NVML (ctypes on the
+    driver's libnvidia-ml) while the timed region runs (a few-millisecond region still
+    gets tens of samples); nvidia-smi as a fallback."""
 
     # nvmlClocksEventReasons bits
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
@@ -194,7 +197,7 @@ class ClockSampler:
             if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0:
                 r = reasons.value if get_reasons(self.handle, ctypes.byref(reasons)) == 0 else 0
                 self.samples.append((float(mhz.value), int(r)))
-            time.sleep(0.002)
+            time.sleep(0.0002)
 
     def start(self):
         try:
@@ -548,51 +551,87 @@ def run_host_sweep(args, w, metric):
 
 
 # ----------------------------------------------------------------------------- large-M GEMMs (context object)
-def large_m_gemms(dev, pk, reps=10):
-    """Gate-up and down grouped GEMMs of the prefill and large workloads, timed
-    alone (CUDA events on the launch stream), plus a library FP8 GEMM for context."""
+def tensor_peak_tflops(pk, fmt):
+    """Dense tensor peak of a format: the measured bf16 burst times the nominal ratio of the
+    format's rate to bf16 (FP8 and FP8 with float32 scales 2x, NVFP4 6x: 4.5 / 13.5 vs 2.25 PF)."""
+    return pk["bf16_tflops"] * {"fp8": 2.0, "fp8_f32sf": 2.0, "nvfp4": 6.0, "bf16": 1.0}[fmt]
+
+
+def _format_operands(fmt, x, wt, K):
+    """Quantised (or bf16) activations and tiled weights of one format, and a GEMM closure."""
+    from block_scaled_fp8_route_gb300 import ops
+    if fmt == "bf16":
+        bq = ops.tile_weights(wt.contiguous())
+        return lambda seg, cnt, d: ops.grouped_gemm_bf16_contig(x, bq, seg, cnt, d=d, flags=ops.B_TILED)
+    if fmt == "nvfp4":
+        aq, asf = ops.quantise_act_nvfp4(x, 0)
+        bq, sfb, b_exp = ops.quantise_weight_nvfp4(wt)
+        bq = ops.tile_weights(bq)
+        return lambda seg, cnt, d: ops.grouped_gemm_nvfp4_contig(aq, asf, 0, bq, sfb, b_exp, seg, cnt, d=d,
+                                                                 flags=ops.B_TILED)
+    if fmt == "fp8_f32sf":
+        aq, asf = ops.quantise_act_f32sf(x)
+        bq, sfb = ops.quantise_weight_f32sf(wt)
+        bq = ops.tile_weights(bq)
+        return lambda seg, cnt, d: ops.grouped_gemm_f32sf_contig(aq, asf, bq, sfb, seg, cnt, d=d, flags=ops.B_TILED)
+    aq, asf = ops.quantise_act(x)
+    bq, sf128 = ops.quantise_weight(wt)
+    bq = ops.tile_weights(bq)
+    sfb = ops.prepare_weight_sf(sf128, K)
+    return lambda seg, cnt, d: ops.grouped_gemm_contig(aq, asf, bq, sfb, seg, cnt, d=d, flags=ops.B_TILED)
+
+
+def large_m_gemms(dev, pk, reps=10, fmts=("fp8",)):
+    """Gate-up and down grouped GEMMs of the prefill and large workloads, timed alone (CUDA events
+    on the launch stream), in each operand format against its own tensor peak and byte roofline,
+    plus a library FP8 GEMM for context."""
     from block_scaled_fp8_route_gb300 import ops
     out = {}
-    fp8_peak = 2.0 * pk["bf16_tflops"]
-    for name in ("prefill", "large"):
-        w = W.WORKLOADS[name]
-        ids, _ = W.routing(w, device=dev)
-        bufs = ops.route(ids, w.E, w.layout, w.align)
-        rows = int(bufs.counts.sum().item())
-        active = int((bufs.counts > 0).sum().item())
-        res = {}
-        for tag, (K, N) in enumerate(((w.K, w.N), (w.K2, w.N2))):
-            x = W.activations(W.with_tokens(w, bufs.m_cap), device=dev, K=K, tag=tag)
-            aq, asf = ops.quantise_act(x)
-            del x
-            wt = W.weights(w, device=dev, N=N, K=K, tag=tag)
-            bq, sf128 = ops.quantise_weight(wt)
-            del wt
-            bq = ops.tile_weights(bq)           # the layout MoEPath uses
-            sfb = ops.prepare_weight_sf(sf128, K)
-            d = torch.empty((bufs.m_cap, N), dtype=torch.bfloat16, device=dev)
-            for _ in range(3):
-                ops.grouped_gemm_contig(aq, asf, bq, sfb, bufs.seg_start, bufs.counts, d=d, flags=ops.B_TILED)
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
-            e0.record()
-            for _ in range(reps):
-                ops.grouped_gemm_contig(aq, asf, bq, sfb, bufs.seg_start, bufs.counts, d=d, flags=ops.B_TILED)
-            e1.record()
-            torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1) / reps
-            tf = 2.0 * rows * N * K / (ms / 1e3) / 1e12
-            qb, sb = operand_bytes(K, "fp8")
-            nbytes = active * weight_bytes(N, K, "fp8") + rows * (qb + sb + 2 * N)
-            rf = binding_roofline(2.0 * rows * N * K, nbytes, ms, fp8_peak, pk["hbm_gbs"])
-            res["gate_up" if tag == 0 else "down"] = {"K": K, "N": N, "ms": ms, "tflops": tf, "frac": tf / fp8_peak,
-                                                      "bytes": nbytes, "bound": rf["bound"],
-                                                      "roofline_frac": rf["roofline_frac"]}
-            del aq, asf, bq, sf128, sfb, d
-            torch.cuda.empty_cache()
-        out[name] = {"routed_rows": rows, **res}
-    out["fp8_peak_tflops"] = fp8_peak
-    out["fp8_peak_src"] = f"2 x bf16 burst ({pk['src']})"
+    for fmt in fmts:
+        peak = tensor_peak_tflops(pk, fmt)
+        res_f = {}
+        for name in ("prefill", "large"):
+            w = W.WORKLOADS[name]
+            ids, _ = W.routing(w, device=dev)
+            bufs = ops.route(ids, w.E, w.layout, w.align)
+            rows = int(bufs.counts.sum().item())
+            active = int((bufs.counts > 0).sum().item())
+            res = {}
+            for tag, (K, N) in enumerate(((w.K, w.N), (w.K2, w.N2))):
+                x = W.activations(W.with_tokens(w, bufs.m_cap), device=dev, K=K, tag=tag)
+                wt = W.weights(w, device=dev, N=N, K=K, tag=tag)
+                gemm = _format_operands(fmt, x, wt, K)
+                del x, wt
+                torch.cuda.empty_cache()
+                d = torch.empty((bufs.m_cap, N), dtype=torch.bfloat16, device=dev)
+                for _ in range(3):
+                    gemm(bufs.seg_start, bufs.counts, d)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+                e0.record()
+                for _ in range(reps):
+                    gemm(bufs.seg_start, bufs.counts, d)
+                e1.record()
+                torch.cuda.synchronize()
+                assert ops.device_error() == 0
+                ms = e0.elapsed_time(e1) / reps
+                tf = 2.0 * rows * N * K / (ms / 1e3) / 1e12
+                qb, sb = operand_bytes(K, fmt)
+                nbytes = active * weight_bytes(N, K, fmt) + rows * (qb + sb + 2 * N)
+                rf = binding_roofline(2.0 * rows * N * K, nbytes, ms, peak, pk["hbm_gbs"])
+                res["gate_up" if tag == 0 else "down"] = {"K": K, "N": N, "ms": ms, "tflops": tf, "frac": tf / peak,
+                                                          "bytes": nbytes, "bound": rf["bound"],
+                                                          "roofline_frac": rf["roofline_frac"]}
+                del gemm, d
+                torch.cuda.empty_cache()
+            res_f[name] = {"routed_rows": rows, **res}
+        res_f["tensor_peak_tflops"] = peak
+        res_f["tensor_peak_src"] = f"{tensor_peak_tflops(pk, fmt) / pk['bf16_tflops']:g} x bf16 burst ({pk['src']})"
+        out[fmt] = res_f
+    if "fp8" in out:   # the FP8 entry keeps its historical flat layout
+        f = out.pop("fp8")
+        out.update({"prefill": f["prefill"], "large": f["large"], "fp8_peak_tflops": f["tensor_peak_tflops"],
+                    "fp8_peak_src": f["tensor_peak_src"]})
     try:   # library FP8 GEMM (cuBLASLt through torch) for context only
         n = 8192
         a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
@@ -888,7 +927,7 @@ def main():
     if rank == 0 and world == 1 and w.name == "decode" and args.fmt == "fp8" and not args.no_large_m:
         del path
         torch.cuda.empty_cache()
-        large_m = large_m_gemms(dev, pk)
+        large_m = large_m_gemms(dev, pk, fmts=("fp8", "nvfp4", "bf16", "fp8_f32sf"))
     if rank == 0:
         cfg = workload_config(w, args.fmt)
         line = {

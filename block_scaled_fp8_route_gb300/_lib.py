@@ -21,6 +21,7 @@ SIGNATURES = {
     "bsf_version": (_c_int, []),
     "bsf_get_device_error": (_c_int, [ctypes.POINTER(ctypes.c_int32), _c_int, _p]),
     "bsf_quantise_act": (_c_int, [_p, _i64, _i64, _p, _p, _i64, _p]),
+    "bsf_quantise_act_rows": (_c_int, [_p, _i64, _i64, _p, _p, _p, _p, _i64, _p]),
     "bsf_quantise_weight": (_c_int, [_p, _i64, _i64, _i64, _p, _p, _p]),
     "bsf_prepare_weight_sf": (_c_int, [_p, _i64, _i64, _i64, _p, _p]),
     "bsf_route_workspace_bytes": (_size, [_i64, _i64, _i64]),

@@ -224,6 +224,18 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* tile_start, const 
   return r;
 }
 
+// acc[j] += partial[j] * scale[j] for 32 columns, two per packed FP32x2 FMA (each half rounded once,
+// as fmaf); the scales come from shared memory as float4 broadcasts.
+__device__ __forceinline__ void promote32(float* acc, const uint32_t (&r)[32], const float* scale) {
+#pragma unroll
+  for (int j4 = 0; j4 < 8; ++j4) {
+    const float4 s4 = reinterpret_cast<const float4*>(scale)[j4];
+    fma2_f32(acc[4 * j4], acc[4 * j4 + 1], __uint_as_float(r[4 * j4]), __uint_as_float(r[4 * j4 + 1]), s4.x, s4.y);
+    fma2_f32(acc[4 * j4 + 2], acc[4 * j4 + 3], __uint_as_float(r[4 * j4 + 2]), __uint_as_float(r[4 * j4 + 3]), s4.z,
+             s4.w);
+  }
+}
+
 // Bounded wait that ignores the abort flag (used while draining at exit).
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
@@ -608,6 +620,10 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
         const Tile tl = decode_tile(t, tile_start, exp_row0, exp_cnt, E, nit, TOK);
         // this warp group's token columns gt0 .. gt0 + kGT - 1 of the tile
         constexpr int kGT = TOK / C::kEpiGroups;
+        // the 128-token tile (large batches) reads the column scales from shared memory as float4
+        // broadcasts and uses packed FP32x2 FMAs; the small tiles (register-capped, HBM-bound) keep
+        // the per-column shuffle
+        constexpr bool kSmemScales = TOK == 128;
         const int gt0 = group * kGT;
         float accv[kGT];
 #pragma unroll
@@ -636,6 +652,14 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
             q1[i] = q1[i + 1];
           }
           fetch(kb + 4, qb[3], q0[3], q1[3]);
+          // column j's scale sB * sA[token j] is the same for every row (lane): lane j computes it once
+          // into the warp's scratch, and every lane reads it back as a float4 broadcast
+          float* sc = reinterpret_cast<float*>(buf);
+          if constexpr (kSmemScales) {
+            sc[lane] = sb * sa0;
+            if constexpr (kGT > 32) sc[32 + lane] = sb * sa1;
+            __syncwarp();
+          }
           if (!warp_wait(&acc_full[acc], acc_phase, abort_flag, p.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * TOK + gt0;
@@ -643,21 +667,29 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
           if (gt0 < tl.ntok) {
             tmem_ld_x32(taddr, r);
             tmem_wait_ld();
+            if constexpr (kSmemScales) {
+              promote32(accv, r, sc);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              accv[j] = fmaf(__uint_as_float(r[j]), sb * __shfl_sync(0xffffffffu, sa0, j), accv[j]);
+              for (int j = 0; j < 32; ++j)
+                accv[j] = fmaf(__uint_as_float(r[j]), sb * __shfl_sync(0xffffffffu, sa0, j), accv[j]);
+            }
           }
           if constexpr (kGT > 32) {
           if (tl.ntok > gt0 + 32) {
             tmem_ld_x32(taddr + 32, r);
             tmem_wait_ld();
+            if constexpr (kSmemScales) {
+              promote32(accv + 32, r, sc + 32);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              accv[32 + j] = fmaf(__uint_as_float(r[j]), sb * __shfl_sync(0xffffffffu, sa1, j), accv[32 + j]);
+              for (int j = 0; j < 32; ++j)
+                accv[32 + j] = fmaf(__uint_as_float(r[j]), sb * __shfl_sync(0xffffffffu, sa1, j), accv[32 + j]);
+            }
           }
           }
           tc_fence_before();
-          __syncwarp();
+          __syncwarp();         // (the scratch is rewritten next stage)
           if (lane == 0) mbar_arrive(&acc_empty[acc]);
           if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1u; }
         }

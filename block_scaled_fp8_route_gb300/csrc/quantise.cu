@@ -14,9 +14,12 @@ namespace {
 
 // One warp per (row, group of four 128-wide K-blocks): lane l covers
 // elements 16 l .. 16 l + 15 of the 512-wide group, i.e. block l / 8.
+// With row_token (a packed operand's token_of_row) only rows t < *rows_used with row_token[t] >= 0
+// are quantised; the others are left unwritten.
 __global__ void __launch_bounds__(256) quantise_act_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t K,
                                                            uint8_t* __restrict__ q, int32_t* __restrict__ sf,
-                                                           int64_t sf_ld) {
+                                                           int64_t sf_ld, const int32_t* __restrict__ row_token,
+                                                           const int32_t* __restrict__ rows_used) {
   pdl_launch_dependents();     // a dependent GEMM may be scheduled now; it waits for completion
   const int64_t n_groups = (K + 511) / 512;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -24,6 +27,7 @@ __global__ void __launch_bounds__(256) quantise_act_kernel(const uint16_t* __res
   if (gw >= T * n_groups) return;
   const int64_t t = gw / n_groups;
   const int64_t g = gw - t * n_groups;
+  if (row_token != nullptr && (t >= __ldg(rows_used) || __ldg(row_token + t) < 0)) return;   // whole warp
   const int64_t k0 = g * 512 + lane * 16;
   const bool active = k0 < K;
 
@@ -192,7 +196,23 @@ extern "C" bsf_status bsf_quantise_act(const void* x, int64_t T, int64_t K, uint
   const int64_t blocks = (warps * 32 + 255) / 256;
   if (blocks > INT32_MAX) return BSF_ERR_UNSUPPORTED;
   quantise_act_kernel<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint16_t*>(x), T, K, q, sf, sf_ld);
+      static_cast<const uint16_t*>(x), T, K, q, sf, sf_ld, nullptr, nullptr);
+  return launch_status();
+}
+
+extern "C" bsf_status bsf_quantise_act_rows(const void* x, int64_t T, int64_t K, const int32_t* token_of_row,
+                                            const int32_t* rows_used, uint8_t* q, int32_t* sf, int64_t sf_ld,
+                                            bsf_stream_t stream) {
+  if (T < 0 || K <= 0 || K % 128 != 0) return BSF_ERR_INVALID_ARGUMENT;
+  if (T == 0) return BSF_OK;
+  if (!x || !q || !sf || !token_of_row || !rows_used) return BSF_ERR_INVALID_ARGUMENT;
+  if (sf_ld < T || sf_ld % 4 != 0) return BSF_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return BSF_ERR_MISALIGNED;
+  const int64_t warps = T * ((K + 511) / 512);
+  const int64_t blocks = (warps * 32 + 255) / 256;
+  if (blocks > INT32_MAX) return BSF_ERR_UNSUPPORTED;
+  quantise_act_kernel<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint16_t*>(x), T, K, q, sf, sf_ld, token_of_row, rows_used);
   return launch_status();
 }
 

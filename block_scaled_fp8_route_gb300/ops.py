@@ -65,16 +65,25 @@ def device_error(clear: bool = True, stream=None) -> int:
     return code.value
 
 
-def quantise_act(x, q=None, sf=None, stream=None):
-    """x bf16 [T, K] -> (q uint8 [T, K], sf int32 [ceil(K/512), sf_ld(T)])."""
+def quantise_act(x, q=None, sf=None, stream=None, rows=None):
+    """x bf16 [T, K] -> (q uint8 [T, K], sf int32 [ceil(K/512), sf_ld(T)]).  ``rows`` = (token_of_row,
+    rows_used) of a packed operand (a RouteBuffers' token_of_row and seg_start[E:]): only its routed
+    rows are quantised, the padding rows of q and sf are left unwritten."""
     T, K = x.shape
     x = x.contiguous()
     if q is None:
         q = torch.empty((T, K), dtype=torch.uint8, device=x.device)
     if sf is None:
         sf = torch.empty((sf_words(K), sf_ld(T)), dtype=torch.int32, device=x.device)
-    _lib.check(_lib.load().bsf_quantise_act(_ptr(x), T, K, _ptr(q), _ptr(sf), sf.shape[1], _stream(stream)),
-               "quantise_act")
+    lib = _lib.load()
+    if rows is None:
+        _lib.check(lib.bsf_quantise_act(_ptr(x), T, K, _ptr(q), _ptr(sf), sf.shape[1], _stream(stream)),
+                   "quantise_act")
+    else:
+        token_of_row, rows_used = rows
+        assert token_of_row.dtype == torch.int32 and token_of_row.numel() >= T and rows_used.dtype == torch.int32
+        _lib.check(lib.bsf_quantise_act_rows(_ptr(x), T, K, _ptr(token_of_row), _ptr(rows_used), _ptr(q), _ptr(sf),
+                                             sf.shape[1], _stream(stream)), "quantise_act_rows")
     return q, sf
 
 

@@ -89,12 +89,12 @@ class MoEPath:
         return (torch.empty((rows, K), dtype=torch.uint8, device=device),
                 torch.empty((ops.sf_words(K), ops.sf_ld(rows)), dtype=torch.int32, device=device))
 
-    def _quantise(self, x, q, sf):
+    def _quantise(self, x, q, sf, rows=None):
         if self.fmt == "fp8_f32sf":
             return ops.quantise_act_f32sf(x, q=q, sf=sf)
         if self.fmt == "nvfp4":
             return ops.quantise_act_nvfp4(x, self.a_exp, q=q, sf=sf)
-        return ops.quantise_act(x, q=q, sf=sf)
+        return ops.quantise_act(x, q=q, sf=sf, rows=rows)
 
     def launches_per_step(self):
         """Kernel launches one ``step`` makes (all of them this library's kernels)."""
@@ -150,7 +150,11 @@ class MoEPath:
             out = self.y2
         elif self.two_gemms:
             with t("quantise2"):
-                self._quantise(h2, self.q2, self.sf2)
+                # FP8: only the routed rows of the packed down-projection input (contiguous layout)
+                rows = None
+                if self.layout == ops.CONTIGUOUS and h2.shape[0] == self.bufs.m_cap:
+                    rows = (self.bufs.token_of_row, self.bufs.seg_start[self.E:])
+                self._quantise(h2, self.q2, self.sf2, rows=rows)
             with t("gemm2"):
                 self.gemm(self.q2, self.sf2, self.w2q, self.sfb2, self.y2, self.b2_exp)
             out = self.y2

@@ -103,6 +103,21 @@ bsf_status bsf_quantise_act(const void* x, int64_t T, int64_t K, uint8_t* q, int
                             bsf_stream_t stream);
 
 /*
+ * bsf_quantise_act_rows — bsf_quantise_act on the routed rows of a packed
+ * operand only (e.g. the input of a second grouped GEMM that shares the
+ * routing): row t is quantised iff t < *rows_used and token_of_row[t] >= 0,
+ * with token_of_row and rows_used = seg_start + E from bsf_route.  The other
+ * rows (segment padding, rows past the last segment) of q and sf are not
+ * written: no stored GEMM output depends on them ("GEMM 执行方式" §4.6 leaves
+ * padding rows uninitialised).  Same arithmetic, layout and checks as
+ * bsf_quantise_act; token_of_row int32 [T] and rows_used int32 [1] are device
+ * pointers.
+ */
+bsf_status bsf_quantise_act_rows(const void* x, int64_t T, int64_t K, const int32_t* token_of_row,
+                                 const int32_t* rows_used, uint8_t* q, int32_t* sf, int64_t sf_ld,
+                                 bsf_stream_t stream);
+
+/*
  * bsf_quantise_weight — expert weights to FP8 with 128 x 128 power-of-two scales
  * (same rule as bsf_quantise_act over 128 x 128 blocks; recipe gran_n = 128).
  *   w      bf16  [E, N, K] row-major.

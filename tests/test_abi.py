@@ -50,6 +50,8 @@ def test_argument_validation_needs_no_device(lib):
                              fake, 1 << 20, nul) == 3
         assert lib.bsf_route_no_alloc(nul, T, kr, 8, 0, 1, fake, fake, fake, fake, nul, 1 << 30, nul, nul, 0, 0, nul,
                                       nul, 0, nul) == 3
+    # row-filtered quantiser: the row filter is required
+    assert lib.bsf_quantise_act_rows(fake, 4, 128, nul, fake, fake, fake, 4, nul) == 1
     # combine with N not a multiple of 8
     assert lib.bsf_combine(nul, 4, nul, nul, 2, 2, 12, nul, nul) == 1
     # dispatch: batch above the single-launch limit is unsupported, K not a multiple of 128 invalid

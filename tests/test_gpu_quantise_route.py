@@ -141,3 +141,28 @@ def test_route_and_scatter_full_size(dev, name):
     sfw = bufs.sfa_packed.cpu().numpy()[:, :used]
     assert np.array_equal(oracle.quantise.unpack_sf(sfw, used, K // 128)[routed], sfb[routed])
     assert ops.device_error() == 0
+
+
+def test_quantise_act_rows_writes_exactly_the_routed_rows():
+    """bsf_quantise_act_rows on a packed operand: routed rows bit-identical to bsf_quantise_act,
+    padding rows and rows past the last segment (data and scale words) left as they were."""
+    dev = require_gpu()
+    w = W.WORKLOADS["prefill"]
+    ids, _ = W.routing(w)
+    bufs = ops.route(ids.to(dev), w.E, w.layout, w.align)
+    K = 1536
+    x = W.activations(W.with_tokens(w, bufs.m_cap), device=dev, K=K, tag=1)
+    q_all, sf_all = ops.quantise_act(x)
+    q = torch.full_like(q_all, 0xA5)
+    sf = torch.full_like(sf_all, -3)
+    ops.quantise_act(x, q=q, sf=sf, rows=(bufs.token_of_row, bufs.seg_start[w.E:]))
+    torch.cuda.synchronize()
+    used = int(bufs.seg_start[-1])
+    tok = bufs.token_of_row[:used]
+    routed = torch.zeros(bufs.m_cap, dtype=torch.bool, device=dev)
+    routed[:used] = tok >= 0
+    assert int(routed.sum()) == w.T * w.kr
+    assert torch.equal(q[routed], q_all[routed])
+    assert torch.equal(sf[:, :bufs.m_cap][:, routed], sf_all[:, :bufs.m_cap][:, routed])
+    assert bool((q[~routed] == 0xA5).all()) and bool((sf[:, :bufs.m_cap][:, ~routed] == -3).all())
+    assert ops.device_error() == 0
