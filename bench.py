@@ -54,6 +54,11 @@ def parse():
                     help="quantise + route as separate launches even where the single-launch dispatch applies")
     ap.add_argument("--no-large-m", action="store_true",
                     help="skip the large-M GEMM measurements added to the decode line")
+    ap.add_argument("--gemm", choices=["gate_up", "down"], default=None,
+                    help="time one grouped GEMM of the workload (prefill / large) instead of the step; with "
+                         "--experts, on the first n experts only (same rows per expert, K and N): the small "
+                         "case of a profiler capture")
+    ap.add_argument("--experts", type=int, default=0)
     return ap.parse_args()
 
 
@@ -747,9 +752,59 @@ def decode_formats(dev, pk, steps=50):
 
 
 # ----------------------------------------------------------------------------- GPU leg
+def run_gemm_case(args, w):
+    """One grouped GEMM of a prefill / large workload (FP8, tiled weights, the step's launch
+    configuration), optionally on its first n experts: --warmup untimed launches, then --steps timed
+    ones (CUDA events); prints one JSON line with the time and the binding roofline."""
+    from block_scaled_fp8_route_gb300 import ops, _lib
+    _lib.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    ids, _ = W.routing(w, device=dev)
+    full = ops.route(ids, w.E, w.layout, w.align)
+    ne = args.experts if args.experts > 0 else w.E
+    counts = full.counts[:ne].clone()
+    seg = torch.zeros(ne + 1, dtype=torch.int32, device=dev)
+    seg[1:] = torch.cumsum((counts + w.align - 1) // w.align * w.align, 0)
+    m = int(seg[-1].item())
+    tag = 0 if args.gemm == "gate_up" else 1
+    K, N = (w.K, w.N) if tag == 0 else (w.K2, w.N2)
+    x = W.activations(W.with_tokens(w, m), device=dev, K=K, tag=tag)
+    wt = W.weights(W.Workload(**{**w.__dict__, "E": ne}), device=dev, N=N, K=K, tag=tag)   # experts 0 .. ne-1
+    gemm = _format_operands("fp8", x, wt, K)
+    del x, wt
+    torch.cuda.empty_cache()
+    d = torch.empty((m, N), dtype=torch.bfloat16, device=dev)
+    for _ in range(args.warmup):
+        gemm(seg, counts, d)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    e0.record()
+    for _ in range(args.steps):
+        gemm(seg, counts, d)
+    e1.record()
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    rows = int(counts.sum().item())
+    active = int((counts > 0).sum().item())
+    qb, sb = operand_bytes(K, "fp8")
+    nbytes = active * weight_bytes(N, K, "fp8") + rows * (qb + sb + 2 * N)
+    flops = 2.0 * rows * N * K
+    roof = binding_roofline(flops, nbytes, ms, tensor_peak_tflops(pk, "fp8"), pk["hbm_gbs"])
+    print(json.dumps({"workload": w.name, "gemm": args.gemm, "experts": ne, "active_experts": active,
+                      "routed_rows": rows, "K": K, "N": N, "ms": ms, "tflops": flops / (ms / 1e3) / 1e12,
+                      "algorithmic_bytes": nbytes, "roofline": roof}), flush=True)
+
+
 def main():
     args = parse()
     w = W.WORKLOADS[args.workload]
+    if args.gemm is not None and args.impl != "reference":
+        assert w.name in ("prefill", "large"), "--gemm applies to the prefill and large workloads"
+        run_gemm_case(args, w)
+        return
     if args.workload == "host" and args.impl != "reference":
         run_host_sweep(args, w, "grouped-GEMM TFLOPS & % FP8 roofline (large M); HBM GB/s & % peak (decode)")
         return
