@@ -158,12 +158,21 @@ struct Cfg {
   static constexpr int kEpiWarps = 4 * kEpiGroups;
   // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue group 0, warps 6-9 SF loaders
   // (epilogue group 1 when kF32Wide), warps 10.. further epilogue groups
-  // WT = 2: one more warp, the waiter, performs every mbarrier wait of the MMA issuer and hands each
-  // stage over through named barrier kHandoffBar, so the issuing thread reads no shared memory
+  // WT = 2: one more warp, the waiter, performs every mbarrier wait of the MMA issuers and hands each
+  // stage over through named barrier kHandoffBar, so no issuing thread reads shared memory; and a
+  // second MMA-issuing warp (kIssuer2Warp) issues weight tile 1's MMAs while warp 1 issues tile 0's.
+  // One issuing thread cannot keep the tensor core busy at N < ~176: each tcgen05.mma costs it ~70
+  // cycles and each stage's hand-off ~100 more, against 72 cycles of tensor work per MMA at N = 144
+  // (isolated issue loop, 8 MMAs per stage: one issuer 681 cycles per stage, two issuers 576 = the
+  // tensor core's own time).
   static constexpr bool kWaiter = WT == 2;
   static constexpr int kWaiterWarp = 2 + kEpiWarps + 4;
+  static constexpr int kIssuers = WT == 2 ? 2 : 1;
+  static constexpr int kIssuer2Warp = kWaiterWarp + 1;
   static constexpr int kHandoffBar = 1;
-  static constexpr int kNumThreads = kF32Wide ? 320 : 32 * (2 + kEpiWarps + 4 + (kWaiter ? 1 : 0));
+  static constexpr int kHandoffThreads = 32 * (1 + kIssuers);   // waiter + issuing warps
+  static constexpr int kNumThreads =
+      kF32Wide ? 320 : 32 * (2 + kEpiWarps + 4 + (kWaiter ? 1 : 0) + (kIssuers - 1));
   static constexpr int kEpiBytes = kEpiWarps * 32 * 32 * 2;   // per epilogue warp: 32 tokens x 32 columns bf16
   static constexpr int kTableBytes = (3 * MAXE + 4) * 4;
   static constexpr int kBarBytes = 512;
@@ -288,17 +297,17 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C::kFp4 ? 5 : 1);      // NVFP4: the MMA commit and the four SF warps
+      mbar_init(&empty[s], (C::kFp4 ? 4 : 0) + C::kIssuers);   // the MMA commits (+ NVFP4: the four SF warps)
     }
     for (int s = 0; s < C::kSfSlots; ++s) {
       mbar_init(&sf_full[s], 4);
-      mbar_init(&sf_empty[s], 1);
+      mbar_init(&sf_empty[s], C::kIssuers);
     }
     for (int s = 0; s < C::kAccBufs; ++s) {
-      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_full[s], C::kIssuers);
       mbar_init(&acc_empty[s], C::kEpiWarps);
     }
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, C::kIssuers);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmap_b);
@@ -427,8 +436,8 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
         drain_wait(&full[stage], phase);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || (C::kIssuers == 2 && warp == C::kIssuer2Warp)) {
+    // ------------------------------------------------------------ MMA issuer(s)
     if (C::kF32 && lane == 0) {
       // one partial accumulator per 128-K stage, alternating between the two TMEM buffers
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
@@ -456,6 +465,11 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
     } else if (!C::kF32) {
       // One stage's MMAs (K = 128 bytes of both operands) into accumulator d_tmem, issued as
       // straight-line code: a branch between two tcgen05.mma instructions stalls the tensor pipe.
+      // With two issuers, each issues the MMAs of its own weight tile w_first (kWN = 1).  The two-tile
+      // items issue in the warp-wide form (every lane runs this code, lane 0 issues).
+      constexpr int kWN = C::kIssuers == 2 ? 1 : WT;
+      const int w_first = warp == 1 ? 0 : 1;
+      const uint32_t lead = lane == 0;
       auto issue_stage = [&](uint32_t stage, uint32_t sf_slot, uint32_t d_tmem, uint32_t mma_n, int kb) {
         const uint32_t sfw = tmem_base + C::kSfBase + sf_slot * C::kSfCols;
         const uint32_t sft = sfw + C::kWSfCols;
@@ -467,16 +481,22 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
           static_assert(!C::kFp4 || TOK == C::kSub, "NVFP4: one MMA sub-tile");
           // (two weight tiles: tile w's words at 16 w + 4k, token words at 16 WT + 4k)
           const uint32_t idesc = idesc_nvf4(kBlockW, mma_n);
-          uint64_t adw[WT];
+          uint64_t adw[kWN];
 #pragma unroll
-          for (int w = 0; w < WT; ++w)
-            adw[w] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + w * kBlockW * kBlockK));
+          for (int ww = 0; ww < kWN; ++ww)
+            adw[ww] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + (w_first + ww) * kBlockW * kBlockK));
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
 #pragma unroll
-            for (int w = 0; w < WT; ++w)
-              mma_nvf4(d_tmem + w * TOK, adw[w] + 2 * k, bdesc + 2 * k, idesc, sfw + 16 * w + 4 * k,
-                       sfw + 16 * WT + C::kTokSfStride * k, (kb | k) != 0);
+            for (int ww = 0; ww < kWN; ++ww) {
+              const int w = w_first + ww;
+              if constexpr (C::kWaiter)
+                mma_nvf4_if(d_tmem + w * TOK, adw[ww] + 2 * k, bdesc + 2 * k, idesc, sfw + 16 * w + 4 * k,
+                            sfw + 16 * WT + C::kTokSfStride * k, (kb | k) != 0, lead);
+              else
+                mma_nvf4(d_tmem + w * TOK, adw[ww] + 2 * k, bdesc + 2 * k, idesc, sfw + 16 * w + 4 * k,
+                         sfw + 16 * WT + C::kTokSfStride * k, (kb | k) != 0);
+            }
           }
         } else {
         // sub-tiles of at most kSub tokens: columns j*kSub.., smem rows j*kSub.., token SF columns j*kSub/32..
@@ -489,40 +509,53 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
           if constexpr (C::kBf16) {
             // four K = 16 steps of 32 bytes inside the swizzled 128-byte rows
             const uint32_t idesc = idesc_bf16(kBlockW, nn);
-            uint64_t adw[WT];
+            uint64_t adw[kWN];
 #pragma unroll
-            for (int w = 0; w < WT; ++w)
-              adw[w] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + w * kBlockW * kBlockK));
+            for (int ww = 0; ww < kWN; ++ww)
+              adw[ww] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + (w_first + ww) * kBlockW * kBlockK));
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
 #pragma unroll
-              for (int w = 0; w < WT; ++w)
-                mma_bf16(d_tmem + w * TOK + j * C::kSub, adw[w] + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+              for (int ww = 0; ww < kWN; ++ww) {
+                const int w = w_first + ww;
+                if constexpr (C::kWaiter)
+                  mma_bf16_if(d_tmem + w * TOK + j * C::kSub, adw[ww] + 2 * k, bd + 2 * k, idesc, (kb | k) != 0, lead);
+                else
+                  mma_bf16(d_tmem + w * TOK + j * C::kSub, adw[ww] + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+              }
             }
           } else {
             const uint32_t idesc = idesc_mxf8_e4m3(kBlockW, nn, kb & 3, kb & 3);
-            uint64_t adw[WT];              // weight tile w of the stage; its accumulator block and SF columns
+            uint64_t adw[kWN];             // weight tile w of the stage; its accumulator block and SF columns
 #pragma unroll
-            for (int w = 0; w < WT; ++w)
-              adw[w] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + w * kBlockW * kBlockK));
+            for (int ww = 0; ww < kWN; ++ww)
+              adw[ww] = smem_desc_k_sw128(smem_u32(stage_b + stage * C::kStageB + (w_first + ww) * kBlockW * kBlockK));
 #pragma unroll
             for (int k = 0; k < kBlockK / 32; ++k) {
               // advance 32 bytes (one K=32 step of FP8) inside the swizzled 128-byte rows
 #pragma unroll
-              for (int w = 0; w < WT; ++w)
-                mma_mxf8(d_tmem + w * TOK + j * C::kSub, adw[w] + 2 * k, bd + 2 * k, idesc, sfw + 4 * w,
-                         sft + j * 8, (kb | k) != 0);
+              for (int ww = 0; ww < kWN; ++ww) {
+                const int w = w_first + ww;
+                if constexpr (C::kWaiter)
+                  mma_mxf8_if(d_tmem + w * TOK + j * C::kSub, adw[ww] + 2 * k, bd + 2 * k, idesc, sfw + 4 * w,
+                              sft + j * 8, (kb | k) != 0, lead);
+                else
+                  mma_mxf8(d_tmem + w * TOK + j * C::kSub, adw[ww] + 2 * k, bd + 2 * k, idesc, sfw + 4 * w,
+                           sft + j * 8, (kb | k) != 0);
+              }
             }
           }
         }
         }
       };
       if constexpr (C::kWaiter) {
-        // The issuing thread reads no shared memory between stages: any load there (an mbarrier
+        // The issuing threads read no shared memory between stages: any load there (an mbarrier
         // wait, even on a completed phase, or a plain flag) lets the tensor pipe drain before the
         // next MMAs (measured: a 4-MMA stage of N = 128 grows from 256 to ~440 cycles).  The waiter
         // warp does every wait and hands each stage over through named barrier kHandoffBar, whose
-        // OR-reduced predicate carries an abort.  The whole warp runs the loop; lane 0 issues.
+        // OR-reduced predicate carries an abort.  Each issuing warp runs the loop whole; its lane 0
+        // issues its weight tile's MMAs and commits, so every barrier the MMAs release counts one
+        // arrival per issuer.
         uint32_t stage = 0, sf_slot = 0, acc = 0;
         bool ok = true;
         for (int t = t_first; t < total_tiles && ok; t += G) {
@@ -531,28 +564,23 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
           const uint32_t d_tmem = tmem_base + acc * C::kAccCols;
           for (int kb = 0; kb < nkb; ++kb) {
             // this stage's data (for kb = 0 also the drained accumulator; per slot the scales) is ready
-            if (named_barrier_or(C::kHandoffBar, 64, false)) { ok = false; break; }
-            if (lane == 0) {
-              tc_fence_after();
-              issue_stage(stage, sf_slot, d_tmem, mma_n, kb);
-              tc_commit(&empty[stage]);
-              if (!C::kBf16 && (kb % C::kKbPerSlot == C::kKbPerSlot - 1 || kb == nkb - 1)) tc_commit(&sf_empty[sf_slot]);
-            }
-            __syncwarp();
+            if (named_barrier_or(C::kHandoffBar, C::kHandoffThreads, false)) { ok = false; break; }
+            tc_fence_after();
+            issue_stage(stage, sf_slot, d_tmem, mma_n, kb);
+            tc_commit_if(&empty[stage], lead);
+            const bool slot_done = !C::kBf16 && (kb % C::kKbPerSlot == C::kKbPerSlot - 1 || kb == nkb - 1);
+            if (slot_done) tc_commit_if(&sf_empty[sf_slot], lead);
             if (++stage == C::kStages) stage = 0;
-            if (!C::kBf16 && (kb % C::kKbPerSlot == C::kKbPerSlot - 1 || kb == nkb - 1))
-              if (++sf_slot == C::kSfSlots) sf_slot = 0;
+            if (slot_done && ++sf_slot == C::kSfSlots) sf_slot = 0;
           }
           if (!ok) break;
-          if (lane == 0) tc_commit(&acc_full[acc]);
-          __syncwarp();
+          tc_commit_if(&acc_full[acc], lead);
           if (++acc == C::kAccBufs) acc = 0;
         }
-        // wait for every MMA issued by this thread before TMEM can be released
-        if (lane == 0) {
-          tc_commit(mma_done);
-          drain_wait(mma_done, 0);
-        }
+        // wait for every MMA issued by this warp's lane 0 (and, through the barrier's count, by the
+        // other issuer) before TMEM can be released
+        tc_commit_if(mma_done, lead);
+        if (lane == 0) drain_wait(mma_done, 0);
       } else if (lane == 0) {
       uint32_t stage = 0, phase = 0, sf_slot = 0, sf_phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
@@ -597,7 +625,7 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
         bool good = kb != 0 || warp_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.err);
         if (good && !C::kBf16 && kb % C::kKbPerSlot == 0) good = warp_wait(&sf_full[sf_slot], sf_phase, abort_flag, p.err);
         if (good) good = warp_wait(&full[stage], phase, abort_flag, p.err);
-        if (named_barrier_or(C::kHandoffBar, 64, !good)) { ok = false; break; }
+        if (named_barrier_or(C::kHandoffBar, C::kHandoffThreads, !good)) { ok = false; break; }
         if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         if (!C::kBf16 && (kb % C::kKbPerSlot == C::kKbPerSlot - 1 || kb == nkb - 1))
           if (++sf_slot == C::kSfSlots) { sf_slot = 0; sf_phase ^= 1u; }
