@@ -19,8 +19,9 @@
 //   large FP8 batches take 256-row items (two 128-row weight tiles sharing
 //   one token chunk, one MMA per weight tile per K-step);
 // * warp roles: warp 0 TMA producer, warp 1 MMA issuer + TMEM owner,
-//   warps 2-5 epilogue, warps 6-9 scale-factor loaders (warps 10-13: a
-//   second epilogue group for the 256-row items);
+//   warps 2-5 epilogue, warps 6-9 scale-factor loaders (256-row items:
+//   warps 10-13 a second epilogue group, warp 14 the waiter that performs the
+//   issuers' mbarrier waits, warp 15 a second MMA issuer);
 // * weights either row-major [E, N, K] or tiled (each 128 x 128-byte TMA box
 //   one contiguous 16 KB run, BSF_B_TILED);
 // * operands: K-major, 128-byte swizzled tiles of 128 K (TMA), STAGES-deep
@@ -43,6 +44,7 @@ constexpr int kBlockW = 128;        // weight rows per tile (MMA M)
 constexpr int kBlockK = 128;        // K per pipeline stage (one 128-byte swizzle row of FP8)
 constexpr int kMaxExperts = 1024;
 constexpr int kBigTok = 224;        // token tile of the large-segment variant
+constexpr int kWideTok = 160;       // token chunk of the four-stage 256-row items (at most 256 experts)
 constexpr int kHostTok = 448;       // token tile of the host-weight (K-outer / M-inner) variant
 constexpr int kFmtFp8 = 0;          // E4M3 operands, UE8M0 scales per 128 K (kind::mxf8f6f4, 1X)
 constexpr int kFmtNvfp4 = 1;        // E2M1 operands, UE4M3 scales per 16 K (kind::mxf4nvf4, 4X)
@@ -93,6 +95,11 @@ struct GemmArgs {
 // into shared memory then cover 1.47x the MMA work of the 128 x 224 tile ((256 + 224) bytes per
 // 256 x 224 products against (128 + 224) per 128 x 224), which is what a latency-bound load
 // pipeline needs; the price is that the epilogue of one item no longer overlaps the next item's MMAs.
+// With at most 256 experts the items are 256 x 160 (kWideTok) instead: the smaller token tile, the
+// smaller tile tables and a half-size epilogue transpose buffer make room for a fourth stage, and
+// with the load pipeline the limit (two MMA issuers keep the tensor core fed) the extra stage in
+// flight pays: same-box A/B, FP8 large gate-up 1713 -> 1534 us, large down 1020 -> 882 us, prefill
+// gate-up 378 -> 367 us; BF16 large gate-up 3160 -> 2826 us; outputs bit-identical.
 template <int TOK, int CPS = 1, int MAXE = kMaxExperts, int FMT = kFmtFp8, int WT = 1>
 struct Cfg {
   static constexpr bool kFp4 = FMT == kFmtNvfp4;
@@ -104,7 +111,7 @@ struct Cfg {
   static constexpr int kKElems = kFp4 ? 256 : kBf16 ? 64 : 128;   // K values per stage
   static constexpr int kKbPerSlot = kFp4 ? 1 : 4;            // stages per SF slot
   // NVFP4 stages also carry the stage's scale words (TMA), which costs one stage of ring depth
-  static constexpr int kStages = WT == 2 ? 3 : kFp4 ? (TOK <= 64 ? 3 : 2)
+  static constexpr int kStages = WT == 2 ? (TOK == 160 ? 4 : 3) : kFp4 ? (TOK <= 64 ? 3 : 2)
                                       : CPS == 2 ? (TOK <= 64 ? (MAXE <= 256 ? 4 : 3) : TOK <= 128 ? 3 : 2)
                                                  : TOK <= 64 ? 8 : TOK <= 224 ? 4 : 2;
   // NVFP4 scale words of one stage in shared memory: weights [4 MMAs][128 rows] int32 (box 128 x 4),
@@ -120,7 +127,8 @@ struct Cfg {
   static constexpr int kSfSlots = (kBf16 || kF32) ? 1 : kFp4 ? (TOK > 128 ? 2 : 4)
                                                              : (CPS == 1 && TOK <= 224 && WT == 1) ? 4 : 2;
   static_assert(kTokSfCols >= 1 && kTokSfCols <= 14, "token SF columns");
-  static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK <= 128 ? 64 : TOK == 192 ? 64 : TOK <= 224 ? 56 : 224;   // token rows per TMA box
+  static constexpr int kBoxRows = TOK <= 64 ? 32 : TOK <= 128 ? 64 : TOK == 160 ? 80 : TOK == 192 ? 64
+                                 : TOK <= 224 ? 56 : 224;   // token rows per TMA box
   // Launched as a programmatic dependent of the preceding kernel (dispatch / route / quantise)
   // only for the small-batch tile: there the launch and prologue overlap that kernel's tail
   // (-0.9 us per graph-replayed decode step, -2 us eager).  The large-tile variants lost
@@ -173,7 +181,10 @@ struct Cfg {
   static constexpr int kHandoffThreads = 32 * (1 + kIssuers);   // waiter + issuing warps
   static constexpr int kNumThreads =
       kF32Wide ? 320 : 32 * (2 + kEpiWarps + 4 + (kWaiter ? 1 : 0) + (kIssuers - 1));
-  static constexpr int kEpiBytes = kEpiWarps * 32 * 32 * 2;   // per epilogue warp: 32 tokens x 32 columns bf16
+  // 160-token two-tile items (at most 256 experts) fit a fourth stage because each epilogue warp
+  // transposes 16 tokens at a time (half the buffer)
+  static constexpr int kEpiTok = (WT == 2 && TOK == 160) ? 16 : 32;
+  static constexpr int kEpiBytes = kEpiWarps * kEpiTok * 32 * 2;   // per epilogue warp: kEpiTok tokens x 32 columns bf16
   static constexpr int kTableBytes = (3 * MAXE + 4) * 4;
   static constexpr int kBarBytes = 512;
   // full + empty per stage, sf_full + sf_empty per SF slot, acc_full + acc_empty per accumulator,
@@ -184,8 +195,11 @@ struct Cfg {
   static_assert(kSfBase + kSfSlots * kSfCols <= 512, "TMEM columns");
   static_assert(kBf16 || kF32 || kWSfCols + (TOK / kSub - 1) * 8 + kSubSfCols <= kSfCols, "SF slot width");
   static_assert(WT == 1 || (WT == 2 && CPS == 1 && (((FMT == kFmtFp8 || FMT == kFmtBf16) && TOK == 224) ||
+                                                    ((FMT == kFmtFp8 || FMT == kFmtBf16) && TOK == 160 && MAXE <= 256) ||
                                                     (FMT == kFmtNvfp4 && (TOK == 128 || TOK == 192)))),
-                "two weight tiles per item, one CTA per SM: FP8 or BF16 with 224 tokens, NVFP4 with 128 or 192");
+                "two weight tiles per item, one CTA per SM: FP8 or BF16 with 224 tokens (or 160 tokens and at "
+                "most 256 experts), NVFP4 with 128 or 192");
+  static_assert(kEpiTok == 32 || !kF32, "FP32-scale epilogue uses the whole buffer");
   static_assert(!kF32 || ((TOK == 64 || TOK == 128) && CPS == 1) || (TOK == 32 && CPS == 2),
                 "FP32-scale tile: 64 or 128 tokens with one CTA per SM, or 32 with two (at most 64 FP32 "
                 "accumulators per thread)");
@@ -637,7 +651,7 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
     const int q = warp & 3;                       // TMEM lane quadrant = weight rows 32q..32q+31
     const int ew = warp < 10 ? warp - 2 : warp - 6;  // epilogue warp 0 .. kEpiWarps-1
     const int group = ew / 4;                          // handles weight tiles group, group + kEpiGroups, ...
-    uint16_t* buf = reinterpret_cast<uint16_t*>(epi) + ew * 32 * 32;
+    uint16_t* buf = reinterpret_cast<uint16_t*>(epi) + ew * C::kEpiTok * 32;
     uint32_t acc = 0, acc_phase = 0;
     if constexpr (C::kF32) {
       // D[token, row] = sum_kb sB[e, nt, kb] * sA[token, kb] * partial_kb: promoted in FP32 registers,
@@ -771,25 +785,28 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[acc]);
         }
-        // buf[j][lane] = D[token c0 + j][weight row 32q + lane]
+        // kEpiTok tokens at a time: buf[jj][lane] = D[token c0 + h + jj][weight row 32q + lane]
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float v = __uint_as_float(r[j]);
-          if constexpr (C::kFp4) v = v * alpha_a * alpha_b;
-          const __nv_bfloat16 h = __float2bfloat16_rn(v);
-          buf[j * 32 + lane] = *reinterpret_cast<const uint16_t*>(&h);
-        }
-        __syncwarp();
+        for (int h = 0; h < 32; h += C::kEpiTok) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int j = (lane >> 2) + 8 * i;
-          if (c0 + j < tl.ntok) {
-            const uint4 v = *reinterpret_cast<const uint4*>(buf + j * 32 + (lane & 3) * 8);
-            uint16_t* dst = p.d + static_cast<int64_t>(tl.tok0 + c0 + j) * N + dcol;
-            *reinterpret_cast<uint4*>(dst) = v;
+          for (int jj = 0; jj < C::kEpiTok; ++jj) {
+            float v = __uint_as_float(r[h + jj]);
+            if constexpr (C::kFp4) v = v * alpha_a * alpha_b;
+            const __nv_bfloat16 hv = __float2bfloat16_rn(v);
+            buf[jj * 32 + lane] = *reinterpret_cast<const uint16_t*>(&hv);
           }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < C::kEpiTok / 8; ++i) {
+            const int jj = (lane >> 2) + 8 * i;
+            if (c0 + h + jj < tl.ntok) {
+              const uint4 v = *reinterpret_cast<const uint4*>(buf + jj * 32 + (lane & 3) * 8);
+              uint16_t* dst = p.d + static_cast<int64_t>(tl.tok0 + c0 + h + jj) * N + dcol;
+              *reinterpret_cast<uint4*>(dst) = v;
+            }
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
       }
       if (ncol == 0) {
@@ -1010,7 +1027,11 @@ extern "C" bsf_status bsf_grouped_gemm_contig(const uint8_t* a, const int32_t* s
     const int64_t max_tiles = (m_cap / kHostTok + E) * (N / 128);
     return launch<kHostTok>(args, a, b, max_tiles, s);
   }
-  if (N % 256 == 0) {   // 256 x 224 items (two weight tiles), one CTA per SM
+  if (N % 256 == 0) {   // 256-row items (two weight tiles), one CTA per SM
+    if (E <= 256) {      // 256 x 160 items, four stages
+      const int64_t max_items = (m_cap / kWideTok + E) * (N / 256);
+      return launch<kWideTok, 1, 256, kFmtFp8, 2>(args, a, b, max_items, s);
+    }
     const int64_t max_items = (m_cap / kBigTok + E) * (N / 256);
     return launch<kBigTok, 1, kMaxExperts, kFmtFp8, 2>(args, a, b, max_items, s);
   }
@@ -1048,6 +1069,10 @@ extern "C" bsf_status bsf_grouped_gemm_masked(const uint8_t* a, const int32_t* s
     return launch<kHostTok>(args, a, b, max_tiles, s);
   }
   if (N % 256 == 0) {
+    if (E <= 256) {
+      const int64_t max_items = E * ((max_m + kWideTok - 1) / kWideTok) * (N / 256);
+      return launch<kWideTok, 1, 256, kFmtFp8, 2>(args, a, b, max_items, s);
+    }
     const int64_t max_items = E * ((max_m + kBigTok - 1) / kBigTok) * (N / 256);
     return launch<kBigTok, 1, kMaxExperts, kFmtFp8, 2>(args, a, b, max_items, s);
   }
@@ -1162,7 +1187,11 @@ extern "C" bsf_status bsf_grouped_gemm_bf16_contig(const void* a, int64_t m_cap,
     const int64_t max_tiles = (m_cap / kHostTok + E) * (N / 128);
     return launch<kHostTok, 1, kMaxExperts, kFmtBf16>(args, ad, bd, max_tiles, s);
   }
-  if (N % 256 == 0) {   // 256 x 224 items (two weight tiles), one CTA per SM
+  if (N % 256 == 0) {   // 256-row items (two weight tiles), one CTA per SM
+    if (E <= 256) {      // 256 x 160 items, four stages
+      const int64_t max_items = (m_cap / kWideTok + E) * (N / 256);
+      return launch<kWideTok, 1, 256, kFmtBf16, 2>(args, ad, bd, max_items, s);
+    }
     const int64_t max_items = (m_cap / kBigTok + E) * (N / 256);
     return launch<kBigTok, 1, kMaxExperts, kFmtBf16, 2>(args, ad, bd, max_items, s);
   }
@@ -1198,6 +1227,10 @@ extern "C" bsf_status bsf_grouped_gemm_bf16_masked(const void* a, const void* b,
     return launch<kHostTok, 1, kMaxExperts, kFmtBf16>(args, ad, bd, max_tiles, s);
   }
   if (N % 256 == 0) {
+    if (E <= 256) {
+      const int64_t max_items = E * ((max_m + kWideTok - 1) / kWideTok) * (N / 256);
+      return launch<kWideTok, 1, 256, kFmtBf16, 2>(args, ad, bd, max_items, s);
+    }
     const int64_t max_items = E * ((max_m + kBigTok - 1) / kBigTok) * (N / 256);
     return launch<kBigTok, 1, kMaxExperts, kFmtBf16, 2>(args, ad, bd, max_items, s);
   }
