@@ -776,16 +776,9 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
       for (int w = group; w < WT; w += C::kEpiGroups) {
       const uint32_t taddr = tacc + w * TOK;
       const int64_t dcol = static_cast<int64_t>(tl.nt * WT + w) * kBlockW + 32 * q + (lane & 3) * 8;
-      for (int c0 = 0; c0 < ncol; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld_x32(taddr + c0, r);
-        tmem_wait_ld();
-        if (w + C::kEpiGroups >= WT && c0 + 32 >= ncol) {   // last chunk in registers: hand the accumulator back
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[acc]);
-        }
-        // kEpiTok tokens at a time: buf[jj][lane] = D[token c0 + h + jj][weight row 32q + lane]
+      // chunk c0's 32 token columns -> bf16, transposed through shared memory, kEpiTok tokens at a
+      // time: buf[jj][lane] = D[token c0 + h + jj][weight row 32q + lane]
+      auto emit = [&](const uint32_t (&r)[32], int c0) {
 #pragma unroll
         for (int h = 0; h < 32; h += C::kEpiTok) {
 #pragma unroll
@@ -807,6 +800,21 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
           }
           __syncwarp();
         }
+      };
+      // last chunk of the item in registers: hand the accumulator back to the MMA issuers
+      auto release_if_last = [&](int c0) {
+        if (w + C::kEpiGroups >= WT && c0 + 32 >= ncol) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
+      };
+      for (int c0 = 0; c0 < ncol; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_x32(taddr + c0, r);
+        tmem_wait_ld_regs(r);
+        release_if_last(c0);
+        emit(r, c0);
       }
       }
       if (ncol == 0) {
