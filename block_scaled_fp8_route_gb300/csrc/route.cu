@@ -31,6 +31,7 @@ constexpr int kMaxExperts = 1024;
 
 __global__ void __launch_bounds__(kThreads) route_count_kernel(const int32_t* __restrict__ ids, int64_t R, int E,
                                                                int32_t* __restrict__ blk_counts, int* err) {
+  pdl_launch_dependents();     // the dependent assign kernel may be scheduled now; it waits for completion
   __shared__ int hist[kMaxExperts];
   __shared__ int bad;
   for (int e = threadIdx.x; e < E; e += kThreads) hist[e] = 0;
@@ -108,20 +109,112 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ 
   }
 }
 
+// Batches of at most kScanInChunks chunks skip route_scan: every assign CTA reads all chunks'
+// histograms (nblk x E words, from L2) and derives its own chunk's per-expert base, the counts and
+// the segment starts itself, with the same integer arithmetic as route_scan; CTA 0 stores counts and
+// seg_start.  One launch fewer (route_scan ran as a single CTA).
+constexpr int kScanInChunks = 64;
+
+// All threads of the CTA.  blk = raw per-chunk histograms [nblk][E]; fills base[e] (assignments of
+// expert e in chunks before `b`), tot[e] (M_e) and seg[0..E] (contiguous: aligned exclusive scan of
+// M_e; masked: slots of max_m rows); returns BSF_DEVERR_* bits seen (CTA-uniform).
+__device__ int scan_chunks(const int32_t* __restrict__ blk, int nblk, int b, int E, int layout, int64_t a_or_m,
+                           int64_t m_cap, int* base, int* tot, int* seg, int* warp_sums) {
+  __shared__ int bad;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) bad = 0;
+  for (int e = tid; e < E; e += kThreads) {
+    int pre = 0, sum = 0;
+    for (int bb = 0; bb < nblk; ++bb) {
+      const int c = blk[static_cast<int64_t>(bb) * E + e];
+      if (bb < b) pre += c;
+      sum += c;
+    }
+    base[e] = pre;
+    tot[e] = sum;
+  }
+  __syncthreads();
+  if (layout == BSF_LAYOUT_MASKED) {
+    for (int e = tid; e < E; e += kThreads) {
+      seg[e] = static_cast<int>(e * a_or_m);
+      if (tot[e] > a_or_m) bad = BSF_DEVERR_MASKED_OVERFLOW;
+    }
+    if (tid == 0) seg[E] = static_cast<int>(E * a_or_m);
+    __syncthreads();
+    return bad;
+  }
+  // contiguous: thread tid owns experts 4 tid .. 4 tid + 3 (E <= 1024 = 4 x kThreads)
+  int64_t len[4], own = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = 4 * tid + j;
+    len[j] = e < E ? (tot[e] + a_or_m - 1) / a_or_m * a_or_m : 0;
+    own += len[j];
+  }
+  int64_t incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = static_cast<int>(incl);
+  __syncthreads();
+  int64_t run = incl - own;
+  for (int w = 0; w < warp; ++w) run += warp_sums[w];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = 4 * tid + j;
+    if (e < E) seg[e] = static_cast<int>(run);
+    run += len[j];
+    if (e == E - 1) {
+      seg[E] = static_cast<int>(run);
+      if (run > m_cap) bad = BSF_DEVERR_SEGMENT;
+    }
+  }
+  __syncthreads();
+  return bad;
+}
+
+// SCAN = false: blk holds each chunk's exclusive per-expert prefix (route_scan's output) and
+// seg_start the segment starts.  SCAN = true: blk holds the raw per-chunk histograms; the CTA derives
+// both itself (scan_chunks) and CTA 0 writes counts and seg_start.
+template <bool SCAN>
 __global__ void __launch_bounds__(kThreads) route_assign_kernel(const int32_t* __restrict__ ids, int64_t R, int kr,
                                                                 int E, int layout, int64_t max_m, int64_t m_cap,
-                                                                const int32_t* __restrict__ blk_base,
-                                                                const int32_t* __restrict__ seg_start,
+                                                                const int32_t* __restrict__ blk_base, int nblk,
+                                                                int32_t* __restrict__ seg_start,
+                                                                int32_t* __restrict__ counts,
                                                                 int32_t* __restrict__ output_index,
                                                                 int32_t* __restrict__ token_of_row, int* err) {
+  // launched as a programmatic dependent: nothing the preceding kernel writes is read before this
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ int smem[];
   int* warp_cnt = smem;                       // [kWarps][E]
-  int* seg = smem + kWarps * E;               // [E]
+  int* seg = smem + kWarps * E;               // [E + 1]
+  int* base = seg + E + 1;                    // [E] (SCAN)
+  int* tot = base + E;                        // [E] (SCAN)
   __shared__ int overflow;
+  __shared__ int warp_sums[kWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int j = threadIdx.x; j < kWarps * E; j += kThreads) warp_cnt[j] = 0;
-  for (int e = threadIdx.x; e < E; e += kThreads) seg[e] = seg_start[e];
   if (threadIdx.x == 0) overflow = 0;
+  if constexpr (SCAN) {
+    const int bad = scan_chunks(blk_base, nblk, static_cast<int>(blockIdx.x), E, layout, max_m, m_cap, base, tot, seg,
+                                warp_sums);
+    if (blockIdx.x == 0) {
+      for (int e = threadIdx.x; e < E; e += kThreads) {
+        counts[e] = layout == BSF_LAYOUT_MASKED ? (tot[e] < max_m ? tot[e] : static_cast<int>(max_m)) : tot[e];
+        seg_start[e] = seg[e];
+      }
+      if (threadIdx.x == 0) {
+        seg_start[E] = seg[E];
+        if (bad) raise_error(err, bad);
+      }
+    }
+  } else {
+    for (int e = threadIdx.x; e < E; e += kThreads) seg[e] = seg_start[e];
+  }
   __syncthreads();
 
   const int64_t sub0 = static_cast<int64_t>(blockIdx.x) * kChunk + warp * kSub;
@@ -138,7 +231,7 @@ __global__ void __launch_bounds__(kThreads) route_assign_kernel(const int32_t* _
   __syncthreads();
   // exclusive prefix over the warps, on top of this chunk's base per expert
   for (int e = threadIdx.x; e < E; e += kThreads) {
-    int run = blk_base[static_cast<int64_t>(blockIdx.x) * E + e];
+    int run = SCAN ? base[e] : blk_base[static_cast<int64_t>(blockIdx.x) * E + e];
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
       const int c = warp_cnt[w * E + e];
@@ -187,6 +280,7 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const int32_
                                                                     int32_t* __restrict__ seg_start,
                                                                     int32_t* __restrict__ output_index,
                                                                     int32_t* __restrict__ token_of_row, int* err) {
+  pdl_launch_dependents();     // the dependent fill kernel may be scheduled now; it waits for completion
   __shared__ RouteBlockSmem sm;
   route_in_block(ids, R, E, layout, a_or_m, m_cap, sm, [&](int64_t i, int64_t dest) {
     output_index[i] = static_cast<int32_t>(dest);
@@ -219,6 +313,7 @@ __global__ void __launch_bounds__(kThreads) route_fill_kernel(int E, int64_t m_c
                                                               uint8_t* __restrict__ a_packed,
                                                               int32_t* __restrict__ sfa_packed, int64_t sfa_ld) {
   pdl_launch_dependents();     // a dependent GEMM may be scheduled now; it waits for completion
+  pdl_wait();                  // launched as a dependent of the routing kernel: its outputs are complete
   __shared__ int tok[kFillRows];
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kFillRows;
   const int64_t rows_used = seg_start[E];
@@ -323,21 +418,32 @@ bsf_status route_impl(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E,
     if (nblk > 0) {
       route_count_kernel<<<nblk, kThreads, 0, s>>>(topk_ids, R, e32, blk, err);
     }
-    route_scan_kernel<<<1, 1024, 0, s>>>(blk, nblk, e32, layout, align_or_max_m, m_cap, counts, seg_start, err);
-    if (nblk > 0) {
-      const size_t smem = static_cast<size_t>(kWarps + 1) * E * sizeof(int);
-      route_assign_kernel<<<nblk, kThreads, smem, s>>>(topk_ids, R, static_cast<int>(kr), e32, layout,
-                                                       align_or_max_m, m_cap, blk, seg_start, output_index,
-                                                       token_of_row, err);
+    bsf_status st = BSF_OK;
+    if (nblk <= kScanInChunks) {
+      // (R = 0: one CTA only writes the counts and segment starts)
+      const size_t smem = (static_cast<size_t>(kWarps + 3) * E + 1) * sizeof(int);
+      st = launch_dependent(route_assign_kernel<true>, static_cast<unsigned>(nblk > 0 ? nblk : 1), kThreads, smem, s,
+                            topk_ids, R, static_cast<int>(kr), e32, layout, align_or_max_m, m_cap,
+                            static_cast<const int32_t*>(blk), nblk, seg_start, counts, output_index, token_of_row, err);
+    } else {
+      route_scan_kernel<<<1, 1024, 0, s>>>(blk, nblk, e32, layout, align_or_max_m, m_cap, counts, seg_start, err);
+      const size_t smem = (static_cast<size_t>(kWarps + 1) * E + 1) * sizeof(int);
+      st = launch_dependent(route_assign_kernel<false>, static_cast<unsigned>(nblk), kThreads, smem, s, topk_ids, R,
+                            static_cast<int>(kr), e32, layout, align_or_max_m, m_cap,
+                            static_cast<const int32_t*>(blk), nblk, seg_start, counts, output_index, token_of_row,
+                            err);
     }
+    if (st != BSF_OK) return st;
   }
   const int64_t fill_blocks = (m_cap + kFillRows - 1) / kFillRows;
   if (fill_blocks > 0) {
-    route_fill_kernel<<<static_cast<unsigned>(fill_blocks), kThreads, 0, s>>>(
-        e32, m_cap, counts, seg_start, token_of_row, m_indices, q, sf, sf_ld,
-        fmt == kRowsNvfp4 ? K / 2 : fmt == kRowsBf16 ? 2 * K : K,
+    const bsf_status st = launch_dependent(
+        route_fill_kernel, static_cast<unsigned>(fill_blocks), kThreads, 0, s, e32, m_cap,
+        static_cast<const int32_t*>(counts), static_cast<const int32_t*>(seg_start), token_of_row, m_indices, q, sf,
+        sf_ld, fmt == kRowsNvfp4 ? K / 2 : fmt == kRowsBf16 ? 2 * K : K,
         fmt == kRowsNvfp4 ? K / 64 : fmt == kRowsBf16 ? 0 : fmt == kRowsFp8F32 ? K / 128 : (K + 511) / 512, a_packed,
         sfa_packed, sfa_ld);
+    if (st != BSF_OK) return st;
   }
   return launch_status();
 }
