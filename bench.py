@@ -52,6 +52,9 @@ def parse():
                          "or FP8 with float32 scales")
     ap.add_argument("--no-fused-dispatch", action="store_true",
                     help="quantise + route as separate launches even where the single-launch dispatch applies")
+    ap.add_argument("--no-route-quantise", action="store_true",
+                    help="large FP8 batches: quantise + route with the token-major copy instead of the fused "
+                         "route + quantise-scatter")
     ap.add_argument("--no-large-m", action="store_true",
                     help="skip the large-M GEMM measurements added to the decode line")
     ap.add_argument("--gemm", choices=["gate_up", "down"], default=None,
@@ -118,8 +121,9 @@ def weight_bytes(N, K, fmt):
 
 def step_work(w, counts, placed_rows, fused_dispatch=False, fmt="fp8"):
     """Algorithmic bytes and GEMM flops of one step (valid rows only; padding excluded).
-    With the single-launch dispatch the activations are read once and only the packed
-    rows are written; otherwise the token-major quantised copy is written and re-read."""
+    With the single-launch dispatch or the fused route + quantise-scatter (stage "dispatch") the
+    activations are read once and only the packed rows are written; otherwise the token-major
+    quantised copy is written and re-read."""
     T, K, N, E, kr = w.T, w.K, w.N, w.E, w.kr
     R = T * kr
     qb, sb = operand_bytes(K, fmt)
@@ -710,7 +714,7 @@ def decode_formats(dev, pk, steps=50):
         torch.cuda.synchronize()
         counts = path.bufs.counts.cpu().numpy()
         placed = int(path.bufs.seg_start[-1].item())
-        byts, _ = step_work(w, counts, placed, fused_dispatch=path.fused_dispatch, fmt=fmt)
+        byts, _ = step_work(w, counts, placed, fused_dispatch=path.fused_dispatch or path.route_quantise, fmt=fmt)
         ev = []
         orig = path.gemm
 
@@ -837,7 +841,7 @@ def main():
     expected_m = w.T * w.kr // w.E
     path = MoEPath(w.E, w.kr, w.T, w.K, w.N, wt, layout=w.layout, align_or_max_m=a_or_m, w2_bf16=wt2,
                    device=dev, expected_m=expected_m, fused_dispatch=False if args.no_fused_dispatch else None,
-                   fmt=args.fmt)
+                   fmt=args.fmt, route_quantise=False if args.no_route_quantise else None)
     del wt, wt2
     torch.cuda.empty_cache()
     h2 = W.activations(W.with_tokens(w, path.bufs.m_cap), device=dev, K=w.K2, tag=1) if w.K2 else None
@@ -849,7 +853,8 @@ def main():
     counts = path.bufs.counts.cpu().numpy()
     placed = int(path.bufs.seg_start[-1].item())
     assert ops.device_error() == 0, "device error during setup"
-    bytes_by_kernel, flops = step_work(w, counts, placed, fused_dispatch=path.fused_dispatch, fmt=args.fmt)
+    bytes_by_kernel, flops = step_work(w, counts, placed, fused_dispatch=path.fused_dispatch or path.route_quantise,
+                                       fmt=args.fmt)
     step_bytes = sum(bytes_by_kernel.values())
 
     for _ in range(args.warmup):

@@ -31,6 +31,8 @@ SIGNATURES = {
                                     _p, _p, _i64, _i64, _p, _p, _i64, _p]),
     "bsf_dispatch": (_c_int, [_p, _i64, _i64, _p, _i64, _i64, _c_int, _i64, _p, _p, _p, _p, _p, _i64,
                               _p, _p, _i64, _p]),
+    "bsf_route_quantise": (_c_int, [_p, _i64, _i64, _p, _i64, _i64, _c_int, _i64, _p, _p, _p, _p, _p, _i64,
+                                    _p, _p, _i64, _p, _size, _p]),
     "bsf_grouped_gemm_contig": (_c_int, [_p, _p, _i64, _i64, _p, _p, _p, _p, _p, _i64, _i64, _i64, _c_int, _p]),
     "bsf_grouped_gemm_masked": (_c_int, [_p, _p, _i64, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _c_int, _p]),
     "bsf_combine": (_c_int, [_p, _i64, _p, _p, _i64, _i64, _i64, _p, _p]),

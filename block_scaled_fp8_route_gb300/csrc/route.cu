@@ -18,6 +18,7 @@
 //   route_fill    per packed row: padding marks, m_indices, row + SF copy (grid: rows)
 #include "common.cuh"
 #include "host_utils.h"
+#include "quant_math.cuh"
 #include "route_block.cuh"
 
 namespace bsf {
@@ -363,6 +364,76 @@ __global__ void __launch_bounds__(kThreads) route_fill_kernel(int E, int64_t m_c
   }
 }
 
+// bsf_route_quantise: one warp per (token t, 512-wide K group g).  The token's bf16 row segment is
+// read once, quantised with the arithmetic of quantise_act_kernel (quant_math.cuh, so the bytes are
+// the same), and its E4M3 codes and scale word are written to each of the token's k_r packed rows
+// (output_index from the assign kernel; -1 = dropped).  Launched as a programmatic dependent of the
+// routing kernels; only the loads of x are issued before the wait.
+__global__ void __launch_bounds__(kThreads) quantise_scatter_kernel(const uint16_t* __restrict__ x, int64_t T,
+                                                                    int64_t K, int kr,
+                                                                    const int32_t* __restrict__ output_index,
+                                                                    uint8_t* __restrict__ a_packed,
+                                                                    int32_t* __restrict__ sfa_packed, int64_t sfa_ld) {
+  pdl_launch_dependents();     // a dependent GEMM may be scheduled now; it waits for completion
+  const int64_t n_groups = (K + 511) / 512;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const bool in_range = gw < T * n_groups;        // warp-uniform
+  const int64_t t = in_range ? gw / n_groups : 0;
+  const int64_t g = in_range ? gw - t * n_groups : 0;
+  const int64_t k0 = g * 512 + lane * 16;
+  const bool active = in_range && k0 < K;
+  uint4 ra = make_uint4(0, 0, 0, 0), rb = ra;
+  if (active) {                                   // x is not written by the routing kernels
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * K + k0);
+    ra = __ldg(src);
+    rb = __ldg(src + 1);
+  }
+  pdl_wait();                                     // output_index is complete
+  if (!in_range) return;
+  const int dest_l = lane < kr ? output_index[t * kr + lane] : -1;
+  float v[16];
+  float amax = 0.f;
+  if (active) {
+    float fa[8], fb[8];
+    bf16x8_to_float(ra, fa);
+    bf16x8_to_float(rb, fb);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[i] = fa[i];
+      v[8 + i] = fb[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  }
+  // max over the 8 lanes of this K-block
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+  const int e = block_exponent(amax);
+  uint4 out = make_uint4(0, 0, 0, 0);
+  if (active) {
+    const float s = inv_pow2(e);
+    out.x = pack4_e4m3(v[0] * s, v[1] * s, v[2] * s, v[3] * s);
+    out.y = pack4_e4m3(v[4] * s, v[5] * s, v[6] * s, v[7] * s);
+    out.z = pack4_e4m3(v[8] * s, v[9] * s, v[10] * s, v[11] * s);
+    out.w = pack4_e4m3(v[12] * s, v[13] * s, v[14] * s, v[15] * s);
+  }
+  // byte j of the SF word = block j of the group (127 for blocks past K)
+  const uint32_t byte = active ? static_cast<uint32_t>(e + 127) : 127u;
+  const uint32_t b0 = __shfl_sync(0xffffffffu, byte, 0);
+  const uint32_t b1 = __shfl_sync(0xffffffffu, byte, 8);
+  const uint32_t b2 = __shfl_sync(0xffffffffu, byte, 16);
+  const uint32_t b3 = __shfl_sync(0xffffffffu, byte, 24);
+  const int32_t word = static_cast<int32_t>(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24));
+  for (int r = 0; r < kr; ++r) {
+    const int dest = __shfl_sync(0xffffffffu, dest_l, r);   // warp-uniform
+    if (dest < 0) continue;
+    if (active) *reinterpret_cast<uint4*>(a_packed + static_cast<int64_t>(dest) * K + k0) = out;
+    if (lane == 0) sfa_packed[g * sfa_ld + dest] = word;
+  }
+}
+
 }  // namespace
 }  // namespace bsf
 
@@ -554,4 +625,28 @@ extern "C" bsf_status bsf_route_no_alloc(const int32_t* topk_ids, int64_t T, int
   return bsf_route(topk_ids, T, kr, E, layout, align_or_max_m, counts, seg_start, output_index, token_of_row,
                    m_indices, m_cap, q, sf, sf_ld, K, a_packed, sfa_packed, sfa_ld, scratch, kRouteStaticScratchBytes,
                    stream);
+}
+
+extern "C" bsf_status bsf_route_quantise(const void* x, int64_t T, int64_t K, const int32_t* topk_ids, int64_t kr,
+                                         int64_t E, int layout, int64_t align_or_max_m, int32_t* counts,
+                                         int32_t* seg_start, int32_t* output_index, int32_t* token_of_row,
+                                         int32_t* m_indices, int64_t m_cap, uint8_t* a_packed, int32_t* sfa_packed,
+                                         int64_t sfa_ld, void* workspace, size_t workspace_bytes,
+                                         bsf_stream_t stream) {
+  if (!x || !a_packed || !sfa_packed || K <= 0 || K % 128) return BSF_ERR_INVALID_ARGUMENT;
+  if (kr > 32) return BSF_ERR_UNSUPPORTED;      // one lane per assignment of a token
+  if (sfa_ld < m_cap || sfa_ld % 4) return BSF_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(a_packed) || !aligned16(sfa_packed)) return BSF_ERR_MISALIGNED;
+  // routing, segment starts, padding marks and m_indices: bsf_route without a scatter source
+  bsf_status st = bsf_route(topk_ids, T, kr, E, layout, align_or_max_m, counts, seg_start, output_index, token_of_row,
+                            m_indices, m_cap, nullptr, nullptr, 0, K, nullptr, nullptr, 0, workspace, workspace_bytes,
+                            stream);
+  if (st != BSF_OK || T == 0) return st;
+  const int64_t warps = T * ((K + 511) / 512);
+  const int64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
+  if (blocks > INT32_MAX) return BSF_ERR_UNSUPPORTED;
+  return launch_dependent(quantise_scatter_kernel, static_cast<unsigned>(blocks), kThreads, 0,
+                          reinterpret_cast<cudaStream_t>(stream), static_cast<const uint16_t*>(x), T, K,
+                          static_cast<int>(kr), static_cast<const int32_t*>(output_index), a_packed, sfa_packed,
+                          sfa_ld);
 }

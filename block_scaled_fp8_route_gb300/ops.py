@@ -211,6 +211,25 @@ def dispatch(x, topk_ids, E, layout, align_or_max_m, bufs=None, stream=None):
     return bufs
 
 
+def route_quantise_supported(kr):
+    return kr <= 32
+
+
+def route_quantise(x, topk_ids, E, layout, align_or_max_m, bufs=None, stream=None):
+    """Quantise + route + scatter for batches of any size (routing kernels, then each token's row
+    quantised once and written to its k_r packed rows); returns a RouteBuffers."""
+    T, K = x.shape
+    kr = topk_ids.shape[1]
+    if bufs is None:
+        bufs = RouteBuffers(T, kr, E, layout, align_or_max_m, K=K, device=x.device)
+    _lib.check(_lib.load().bsf_route_quantise(
+        _ptr(x.contiguous()), T, K, _ptr(topk_ids.contiguous()), kr, E, layout, align_or_max_m,
+        _ptr(bufs.counts), _ptr(bufs.seg_start), _ptr(bufs.output_index), _ptr(bufs.token_of_row),
+        _ptr(bufs.m_indices), bufs.m_cap, _ptr(bufs.a_packed), _ptr(bufs.sfa_packed), bufs.sfa_packed.shape[1],
+        _ptr(bufs.workspace), bufs.workspace.numel(), _stream(stream)), "route_quantise")
+    return bufs
+
+
 def grouped_gemm_contig(a, sfa, b, sfb, seg_start, counts, d=None, flags=0, stream=None):
     """a uint8 [m_cap, K], b uint8 [E, N, K] -> d bf16 [m_cap, N] (segment rows written)."""
     m_cap, K = a.shape

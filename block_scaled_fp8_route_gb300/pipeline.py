@@ -32,7 +32,7 @@ class MoEPath:
 
     def __init__(self, E, kr, T, K, N, w_bf16, layout=ops.CONTIGUOUS, align_or_max_m=1, w2_bf16=None,
                  device="cuda", weights_on_host=False, expected_m=0, fused_dispatch=None, fmt="fp8", a_exp=0,
-                 tiled_weights=True):
+                 tiled_weights=True, route_quantise=None):
         self.E, self.kr, self.T, self.K, self.N = E, kr, T, K, N
         self.layout, self.align_or_max_m = layout, align_or_max_m
         self.expected_m = expected_m
@@ -50,6 +50,10 @@ class MoEPath:
         self.fused_dispatch = ops.dispatch_supported(T, kr, E) if fused_dispatch is None else fused_dispatch
         if fmt in ("bf16", "fp8_f32sf"):
             self.fused_dispatch = False          # the route scatters the rows (bf16, or e4m3 + float32 scales)
+        # FP8 batches above the single-launch limit: route, then quantise each token once into its k_r
+        # packed rows (bsf_route_quantise) instead of quantise + route with a token-major copy
+        auto_rq = fmt == "fp8" and not self.fused_dispatch and ops.route_quantise_supported(kr)
+        self.route_quantise = auto_rq if route_quantise is None else (route_quantise and auto_rq)
         m = self.bufs.m_cap
         self.q, self.sf = self._act_buffers(T, K, device)
         self.y = torch.empty((max(m, 1), N), dtype=torch.bfloat16, device=device)
@@ -98,12 +102,17 @@ class MoEPath:
 
     def launches_per_step(self):
         """Kernel launches one ``step`` makes (all of them this library's kernels)."""
+        R = self.T * self.kr
+        if ops.dispatch_supported(self.T, self.kr, self.E):
+            route = 2                                              # route_small + fill
+        else:
+            route = 3 + (1 if (R + 2047) // 2048 > 64 else 0)      # count + assign + fill (+ scan)
         if self.fused_dispatch:
             n = 1                                                  # dispatch
+        elif self.route_quantise:
+            n = route + 1                                          # routing + quantise-scatter
         else:
-            small = ops.dispatch_supported(self.T, self.kr, self.E)
-            quant = 0 if self.fmt == "bf16" else 1
-            n = quant + (2 if small else 4)                        # quantise + route (+ fill)
+            n = (0 if self.fmt == "bf16" else 1) + route           # quantise + routing
         n += 1                                                     # grouped GEMM
         if self.two_gemms:
             n += 1 if self.fmt == "bf16" else 2                    # (quantise of h2 +) second GEMM
@@ -172,6 +181,9 @@ class MoEPath:
         elif self.fused_dispatch:
             with t("dispatch"):
                 ops.dispatch(x, topk_ids, self.E, self.layout, self.align_or_max_m, bufs=self.bufs)
+        elif self.route_quantise:
+            with t("dispatch"):
+                ops.route_quantise(x, topk_ids, self.E, self.layout, self.align_or_max_m, bufs=self.bufs)
         elif self.fmt == "bf16":
             with t("route"):
                 ops.route(topk_ids, self.E, self.layout, self.align_or_max_m, q=x, bufs=self.bufs, fmt="bf16")

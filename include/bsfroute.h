@@ -188,6 +188,32 @@ bsf_status bsf_route(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E, 
                      size_t workspace_bytes, bsf_stream_t stream);
 
 /*
+ * bsf_route_quantise — bsf_quantise_act + bsf_route with the scatter, fused
+ * for batches of any size: route (as bsf_route), then one warp per (token,
+ * 512-wide K group) reads the token's bf16 row segment ONCE, quantises it
+ * (the same arithmetic and bytes as bsf_quantise_act) and writes the codes
+ * and the scale word to each of the token's k_r packed rows.  The token-major
+ * q / sf copies are neither written nor re-read.
+ * "GEMM 执行方式" §4.2-§4.6 (routing, packed layout, ep_scatter);
+ * "CuTeDSL bei Perplexity", MoE dispatch (quantise and copy in one pass);
+ * DeepGEMM article "补偿机制一" (1 x 128 UE8M0 block scales).
+ *   x             bf16 [T, K], K % 128 == 0 (device, caller-owned, read only).
+ *   a_packed      e4m3 [m_cap, K], sfa_packed int32 [ceil(K/512)][sfa_ld],
+ *                 sfa_ld >= m_cap and a multiple of 4 (outputs): routed rows
+ *                 written, padding rows left as they were.
+ *   kr <= 32 (else BSF_ERR_UNSUPPORTED).  x, a_packed and sfa_packed must be
+ *   16-byte aligned (BSF_ERR_MISALIGNED).
+ *   Every other argument, output, device error bit and host-side check as in
+ *   bsf_route; every output is bit-identical to bsf_quantise_act followed by
+ *   bsf_route with the scatter.  Nothing is allocated; asynchronous on stream.
+ */
+bsf_status bsf_route_quantise(const void* x, int64_t T, int64_t K, const int32_t* topk_ids, int64_t kr, int64_t E,
+                              int layout, int64_t align_or_max_m, int32_t* counts, int32_t* seg_start,
+                              int32_t* output_index, int32_t* token_of_row, int32_t* m_indices, int64_t m_cap,
+                              uint8_t* a_packed, int32_t* sfa_packed, int64_t sfa_ld, void* workspace,
+                              size_t workspace_bytes, bsf_stream_t stream);
+
+/*
  * bsf_route_no_alloc — bsf_route without a caller-provided workspace.
  * The pages have no counterpart of this entry point; it exists for callers
  * that cannot call cudaMalloc where they route: serving runtimes that reserve

@@ -166,3 +166,66 @@ def test_quantise_act_rows_writes_exactly_the_routed_rows():
     assert torch.equal(sf[:, :bufs.m_cap][:, routed], sf_all[:, :bufs.m_cap][:, routed])
     assert bool((q[~routed] == 0xA5).all()) and bool((sf[:, :bufs.m_cap][:, ~routed] == -3).all())
     assert ops.device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_a128", "decode", "prefill", "large"])
+def test_route_quantise_matches_oracle(dev, name):
+    """bsf_route_quantise (route, then every token quantised once into its k_r packed rows): routing
+    arrays, packed rows and scale words against the oracle, as for quantise + route."""
+    w = W.WORKLOADS[name]
+    ids, _ = W.routing(w)
+    K = 512 if name in ("prefill", "large") else w.K
+    x = W.activations(W.with_tokens(w, w.T), K=K)
+    a_or_m = w.max_m if w.layout == W.MASKED else w.align
+    bufs = ops.route_quantise(x.to(dev), ids.to(dev), w.E, w.layout, a_or_m)
+    torch.cuda.synchronize()
+    ref = oracle.route.route(ids.numpy(), w.E, w.layout, align=w.align, max_m=w.max_m)
+    _check_route(bufs, ref, w.layout)
+    aq, asf = oracle.quantise.quantise_act(bits16(x))
+    used = ref["rows_used"]
+    routed = ref["token_of_row"] >= 0
+    rows = oracle.route.scatter_rows(aq, ref["token_of_row"])
+    sfb = oracle.route.scatter_rows(asf, ref["token_of_row"], pad_value=127)
+    assert np.array_equal(u8(bufs.a_packed)[:used][routed], rows[routed])
+    sfw = bufs.sfa_packed.cpu().numpy()[:, :used]
+    assert np.array_equal(oracle.quantise.unpack_sf(sfw, used, K // 128)[routed], sfb[routed])
+    assert ops.device_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_route_quantise_equals_quantise_then_route(dev, seed):
+    """Drops (-1), repeated experts, masked overflow, ragged K: every output of the fused path is
+    bit-identical to bsf_quantise_act + bsf_route with the scatter; padding rows stay untouched."""
+    rng = np.random.default_rng(100 + seed)
+    T, kr, E = int(rng.integers(1, 5000)), int(rng.integers(1, 9)), int(rng.integers(1, 300))
+    K = 128 * int(rng.integers(1, 12))
+    ids = torch.as_tensor(rng.integers(-1, E, (T, kr)).astype(np.int32)).to(dev)
+    x = _x(T, K, seed).to(dev)
+    for layout, a in ((ops.CONTIGUOUS, 1), (ops.CONTIGUOUS, 128), (ops.MASKED, max(1, (T * kr) // (2 * E)))):
+        q, sf = ops.quantise_act(x)
+        ref = ops.route(ids, E, layout, a, q=q, sf=sf)
+        got = ops.RouteBuffers(T, kr, E, layout, a, K=K, device=dev)
+        got.a_packed.fill_(0x5A)
+        got.sfa_packed.fill_(-7)
+        ops.route_quantise(x, ids, E, layout, a, bufs=got)
+        torch.cuda.synchronize()
+        assert ops.device_error() == ref_err(layout, ids, E, a)
+        for name in ("counts", "seg_start", "output_index"):
+            assert torch.equal(getattr(got, name), getattr(ref, name)), name
+        used = int(ref.seg_start[-1])
+        assert torch.equal(got.token_of_row[:used], ref.token_of_row[:used])
+        assert torch.equal(got.m_indices[:used], ref.m_indices[:used])
+        routed = torch.zeros(got.m_cap, dtype=torch.bool, device=dev)
+        routed[:used] = ref.token_of_row[:used] >= 0
+        assert torch.equal(got.a_packed[routed], ref.a_packed[routed])
+        assert torch.equal(got.sfa_packed[:, :got.m_cap][:, routed], ref.sfa_packed[:, :got.m_cap][:, routed])
+        assert bool((got.a_packed[~routed] == 0x5A).all())
+        assert bool((got.sfa_packed[:, :got.m_cap][:, ~routed] == -7).all())
+
+
+def ref_err(layout, ids, E, a):
+    """Device error bits the routing of these ids raises (masked overflow only; ids are < E)."""
+    if layout != ops.MASKED:
+        return 0
+    counts = torch.bincount(ids[ids >= 0].long().flatten(), minlength=E)
+    return 0x2 if bool((counts > a).any()) else 0
