@@ -186,7 +186,9 @@ __global__ void __launch_bounds__(kThreads) route_assign_kernel(const int32_t* _
                                                                 int32_t* __restrict__ seg_start,
                                                                 int32_t* __restrict__ counts,
                                                                 int32_t* __restrict__ output_index,
-                                                                int32_t* __restrict__ token_of_row, int* err) {
+                                                                int32_t* __restrict__ token_of_row,
+                                                                int32_t* __restrict__ m_indices, int mark_rows,
+                                                                int* err) {
   // launched as a programmatic dependent: nothing the preceding kernel writes is read before this
   pdl_wait();
   pdl_launch_dependents();
@@ -211,6 +213,18 @@ __global__ void __launch_bounds__(kThreads) route_assign_kernel(const int32_t* _
       if (threadIdx.x == 0) {
         seg_start[E] = seg[E];
         if (bad) raise_error(err, bad);
+      }
+    }
+    if (mark_rows) {
+      // padding rows of experts e = b, b + grid, ...: token -1, owner e (what route_fill does without
+      // a scatter source, so that no fill launch is needed)
+      for (int e = blockIdx.x; e < E; e += gridDim.x) {
+        const int placed = layout == BSF_LAYOUT_MASKED ? (tot[e] < max_m ? tot[e] : static_cast<int>(max_m)) : tot[e];
+        const int64_t end = layout == BSF_LAYOUT_MASKED ? static_cast<int64_t>(seg[e]) + max_m : seg[e + 1];
+        for (int64_t r = static_cast<int64_t>(seg[e]) + placed + threadIdx.x; r < end && r < m_cap; r += kThreads) {
+          token_of_row[r] = -1;
+          if (m_indices) m_indices[r] = e;
+        }
       }
     }
   } else {
@@ -267,7 +281,10 @@ __global__ void __launch_bounds__(kThreads) route_assign_kernel(const int32_t* _
         }
       }
       output_index[i] = static_cast<int32_t>(dest);
-      if (dest >= 0) token_of_row[dest] = static_cast<int32_t>(i / kr);
+      if (dest >= 0) {
+        token_of_row[dest] = static_cast<int32_t>(i / kr);
+        if (SCAN && mark_rows && m_indices) m_indices[dest] = id;
+      }
     }
   }
   __syncthreads();
@@ -482,6 +499,7 @@ bsf_status route_impl(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E,
   const int nblk = static_cast<int>((R + kChunk - 1) / kChunk);
   int32_t* blk = static_cast<int32_t*>(workspace);
   const int e32 = static_cast<int>(E);
+  bool marks_in_assign = false;
   if (R <= kSmallMaxR && E <= kSmallMaxE) {
     route_small_kernel<<<1, kSmallThreads, 0, s>>>(topk_ids, R, static_cast<int>(kr), e32, layout, align_or_max_m,
                                                    m_cap, counts, seg_start, output_index, token_of_row, err);
@@ -491,22 +509,25 @@ bsf_status route_impl(const int32_t* topk_ids, int64_t T, int64_t kr, int64_t E,
     }
     bsf_status st = BSF_OK;
     if (nblk <= kScanInChunks) {
-      // (R = 0: one CTA only writes the counts and segment starts)
+      // (R = 0: one CTA only writes the counts and segment starts).  Without a scatter source the
+      // assign CTAs also mark the padding rows and write m_indices, and no fill kernel follows.
+      marks_in_assign = q == nullptr;
       const size_t smem = (static_cast<size_t>(kWarps + 3) * E + 1) * sizeof(int);
       st = launch_dependent(route_assign_kernel<true>, static_cast<unsigned>(nblk > 0 ? nblk : 1), kThreads, smem, s,
                             topk_ids, R, static_cast<int>(kr), e32, layout, align_or_max_m, m_cap,
-                            static_cast<const int32_t*>(blk), nblk, seg_start, counts, output_index, token_of_row, err);
+                            static_cast<const int32_t*>(blk), nblk, seg_start, counts, output_index, token_of_row,
+                            m_indices, static_cast<int>(marks_in_assign), err);
     } else {
       route_scan_kernel<<<1, 1024, 0, s>>>(blk, nblk, e32, layout, align_or_max_m, m_cap, counts, seg_start, err);
       const size_t smem = (static_cast<size_t>(kWarps + 1) * E + 1) * sizeof(int);
       st = launch_dependent(route_assign_kernel<false>, static_cast<unsigned>(nblk), kThreads, smem, s, topk_ids, R,
                             static_cast<int>(kr), e32, layout, align_or_max_m, m_cap,
                             static_cast<const int32_t*>(blk), nblk, seg_start, counts, output_index, token_of_row,
-                            err);
+                            m_indices, 0, err);
     }
     if (st != BSF_OK) return st;
   }
-  const int64_t fill_blocks = (m_cap + kFillRows - 1) / kFillRows;
+  const int64_t fill_blocks = marks_in_assign ? 0 : (m_cap + kFillRows - 1) / kFillRows;
   if (fill_blocks > 0) {
     const bsf_status st = launch_dependent(
         route_fill_kernel, static_cast<unsigned>(fill_blocks), kThreads, 0, s, e32, m_cap,

@@ -110,7 +110,9 @@ class MoEPath:
         if self.fused_dispatch:
             n = 1                                                  # dispatch
         elif self.route_quantise:
-            n = route + 1                                          # routing + quantise-scatter
+            # (up to 64 chunks the assign kernel marks the padding rows itself: no fill launch)
+            small = ops.dispatch_supported(self.T, self.kr, self.E)
+            n = route + 1 - (0 if small or (R + 2047) // 2048 > 64 else 1)   # routing + quantise-scatter
         else:
             n = (0 if self.fmt == "bf16" else 1) + route           # quantise + routing
         n += 1                                                     # grouped GEMM
