@@ -52,6 +52,14 @@ def test_argument_validation_needs_no_device(lib):
                                       nul, 0, nul) == 3
     # row-filtered quantiser: the row filter is required
     assert lib.bsf_quantise_act_rows(fake, 4, 128, nul, fake, fake, fake, 4, nul) == 1
+    # fused route + quantise: K a multiple of 128, at most 32 routes per token, 16-byte aligned buffers
+    odd = ctypes.c_void_p(264)
+    assert lib.bsf_route_quantise(fake, 4, 100, nul, 2, 4, 0, 1, fake, fake, fake, fake, nul, 8, fake, fake, 8,
+                                  fake, 64, nul) == 1
+    assert lib.bsf_route_quantise(fake, 4, 128, nul, 33, 4, 0, 1, fake, fake, fake, fake, nul, 200, fake, fake, 200,
+                                  fake, 64, nul) == 3
+    assert lib.bsf_route_quantise(odd, 4, 128, nul, 2, 4, 0, 1, fake, fake, fake, fake, nul, 8, fake, fake, 8,
+                                  fake, 64, nul) == 2
     # combine with N not a multiple of 8
     assert lib.bsf_combine(nul, 4, nul, nul, 2, 2, 12, nul, nul) == 1
     # dispatch: batch above the single-launch limit is unsupported, K not a multiple of 128 invalid
