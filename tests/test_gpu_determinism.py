@@ -14,6 +14,10 @@ pytestmark = pytest.mark.gpu
 SMALL_DECODE = W.Workload("decode_small", T=128, kr=8, E=128, K=1024, N=256, layout=W.MASKED, max_m=64, seed=1001)
 SMALL_PREFILL = W.Workload("prefill_small", T=512, kr=8, E=32, K=1024, N=512, layout=W.CONTIGUOUS, align=128,
                            routing="zipf", seed=1002)
+# above the single-launch limit: multi-chunk routing (count -> assign) and, for FP8, the fused
+# route + quantise-scatter path
+MID_PREFILL = W.Workload("prefill_mid", T=4096, kr=8, E=64, K=1024, N=512, layout=W.CONTIGUOUS, align=128,
+                         routing="zipf", seed=1003)
 
 
 @pytest.fixture(scope="module")
@@ -22,7 +26,7 @@ def dev():
 
 
 @pytest.mark.parametrize("fmt", ["fp8", "nvfp4", "bf16", "fp8_f32sf"])
-@pytest.mark.parametrize("w", [SMALL_DECODE, SMALL_PREFILL], ids=["decode", "prefill"])
+@pytest.mark.parametrize("w", [SMALL_DECODE, SMALL_PREFILL, MID_PREFILL], ids=["decode", "prefill", "prefill_mid"])
 def test_twenty_runs_bit_identical(dev, fmt, w):
     x, wt = W.activations(w).to(dev), W.weights(w)
     ids, p = W.routing(w)
