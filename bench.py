@@ -757,8 +757,8 @@ def decode_formats(dev, pk, steps=50):
 
 # ----------------------------------------------------------------------------- GPU leg
 def run_gemm_case(args, w):
-    """One grouped GEMM of a prefill / large workload (FP8, tiled weights, the step's launch
-    configuration), optionally on its first n experts: --warmup untimed launches, then --steps timed
+    """One grouped GEMM of a prefill / large workload (operand format --fmt, tiled weights, the step's
+    launch configuration), optionally on its first n experts: --warmup untimed launches, then --steps timed
     ones (CUDA events); prints one JSON line with the time and the binding roofline."""
     from block_scaled_fp8_route_gb300 import ops, _lib
     _lib.load()
@@ -776,7 +776,7 @@ def run_gemm_case(args, w):
     K, N = (w.K, w.N) if tag == 0 else (w.K2, w.N2)
     x = W.activations(W.with_tokens(w, m), device=dev, K=K, tag=tag)
     wt = W.weights(W.Workload(**{**w.__dict__, "E": ne}), device=dev, N=N, K=K, tag=tag)   # experts 0 .. ne-1
-    gemm = _format_operands("fp8", x, wt, K)
+    gemm = _format_operands(args.fmt, x, wt, K)
     del x, wt
     torch.cuda.empty_cache()
     d = torch.empty((m, N), dtype=torch.bfloat16, device=dev)
@@ -793,11 +793,11 @@ def run_gemm_case(args, w):
     ms = e0.elapsed_time(e1) / args.steps
     rows = int(counts.sum().item())
     active = int((counts > 0).sum().item())
-    qb, sb = operand_bytes(K, "fp8")
-    nbytes = active * weight_bytes(N, K, "fp8") + rows * (qb + sb + 2 * N)
+    qb, sb = operand_bytes(K, args.fmt)
+    nbytes = active * weight_bytes(N, K, args.fmt) + rows * (qb + sb + 2 * N)
     flops = 2.0 * rows * N * K
-    roof = binding_roofline(flops, nbytes, ms, tensor_peak_tflops(pk, "fp8"), pk["hbm_gbs"])
-    print(json.dumps({"workload": w.name, "gemm": args.gemm, "experts": ne, "active_experts": active,
+    roof = binding_roofline(flops, nbytes, ms, tensor_peak_tflops(pk, args.fmt), pk["hbm_gbs"])
+    print(json.dumps({"workload": w.name, "gemm": args.gemm, "fmt": args.fmt, "experts": ne, "active_experts": active,
                       "routed_rows": rows, "K": K, "N": N, "ms": ms, "tflops": flops / (ms / 1e3) / 1e12,
                       "algorithmic_bytes": nbytes, "roofline": roof}), flush=True)
 
