@@ -26,8 +26,12 @@ def test_host_only_calls(lib):
     assert lib.bsf_version() >= 1
     assert lib.bsf_status_string(0) == b"ok"
     assert lib.bsf_status_string(2).startswith(b"pointer")
-    # workspace size is host arithmetic: one int32 per (2048-assignment chunk, expert)
-    assert lib.bsf_route_workspace_bytes(8192, 8, 256) == 32 * 256 * 4
+    # workspace size is host arithmetic: one int32 per (chunk, expert), the chunk the smallest of
+    # 512 / 1024 / 2048 assignments that keeps the batch within 64 chunks (else 2048)
+    assert lib.bsf_route_workspace_bytes(4096, 8, 128) == 64 * 128 * 4       # 32768 / 512
+    assert lib.bsf_route_workspace_bytes(8192, 8, 256) == 64 * 256 * 4       # 65536 / 1024
+    assert lib.bsf_route_workspace_bytes(8193, 8, 256) == 33 * 256 * 4       # 65544 -> 2048-chunks
+    assert lib.bsf_route_workspace_bytes(65536, 8, 16) == 256 * 16 * 4       # 524288 / 2048 (route_scan)
     assert lib.bsf_route_workspace_bytes(1, 1, 4) == 16
     # T * kr above INT32_MAX: refused (0 bytes) without forming the product
     assert lib.bsf_route_workspace_bytes(2**31, 8, 8) == 0

@@ -110,6 +110,20 @@ def test_route_random_with_duplicates_and_drops(dev, seed):
     assert ops.device_error() == 0
 
 
+# the multi-CTA route picks 512-, 1024- or 2048-assignment chunks by batch size (at most 64 chunks,
+# else 2048 and a separate scan): one batch in each regime, each with a ragged last chunk
+@pytest.mark.parametrize("T,kr,E", [(2049, 8, 64), (4000, 8, 300), (5000, 8, 128), (9000, 8, 1024),
+                                    (20001, 8, 256)])
+def test_route_every_chunk_size(dev, T, kr, E):
+    rng = np.random.default_rng(T)
+    ids = rng.integers(-1, E, (T, kr)).astype(np.int32)
+    for layout, a in ((ops.CONTIGUOUS, 128), (ops.MASKED, 2 * T * kr // E + 64)):
+        ref = oracle.route.route(ids, E, layout, align=a, max_m=a)
+        bufs = _route_gpu(dev, ids, E, layout, a)
+        _check_route(bufs, ref, layout)
+    assert ops.device_error() == 0
+
+
 def test_route_masked_overflow_and_bad_id(dev):
     ids = np.array([[0, 1], [0, 1], [0, 2], [1, 0]], dtype=np.int32)
     ref = oracle.route.route(ids, 3, oracle.route.MASKED, max_m=2)
