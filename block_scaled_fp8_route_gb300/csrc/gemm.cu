@@ -181,10 +181,10 @@ struct Cfg {
   static constexpr int kHandoffThreads = 32 * (1 + kIssuers);   // waiter + issuing warps
   static constexpr int kNumThreads =
       kF32Wide ? 320 : 32 * (2 + kEpiWarps + 4 + (kWaiter ? 1 : 0) + (kIssuers - 1));
-  // 160-token two-tile items (at most 256 experts) fit a fourth stage because each epilogue warp
-  // transposes 16 tokens at a time (half the buffer)
-  static constexpr int kEpiTok = (WT == 2 && TOK == 160) ? 16 : 32;
-  static constexpr int kEpiBytes = kEpiWarps * kEpiTok * 32 * 2;   // per epilogue warp: kEpiTok tokens x 32 columns bf16
+  // shared memory of the FP32-scale epilogue (per warp: the partial's column scales, and at the end of
+  // a tile 32 tokens x 32 columns of bf16 for the transposed stores); the other epilogues store
+  // straight from registers
+  static constexpr int kEpiBytes = kF32 ? kEpiWarps * 32 * 32 * 2 : 0;
   static constexpr int kTableBytes = (3 * MAXE + 4) * 4;
   static constexpr int kBarBytes = 512;
   // full + empty per stage, sf_full + sf_empty per SF slot, acc_full + acc_empty per accumulator,
@@ -199,7 +199,6 @@ struct Cfg {
                                                     (FMT == kFmtNvfp4 && (TOK == 128 || TOK == 192)))),
                 "two weight tiles per item, one CTA per SM: FP8 or BF16 with 224 tokens (or 160 tokens and at "
                 "most 256 experts), NVFP4 with 128 or 192");
-  static_assert(kEpiTok == 32 || !kF32, "FP32-scale epilogue uses the whole buffer");
   static_assert(!kF32 || ((TOK == 64 || TOK == 128) && CPS == 1) || (TOK == 32 && CPS == 2),
                 "FP32-scale tile: 64 or 128 tokens with one CTA per SM, or 32 with two (at most 64 FP32 "
                 "accumulators per thread)");
@@ -651,7 +650,7 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
     const int q = warp & 3;                       // TMEM lane quadrant = weight rows 32q..32q+31
     const int ew = warp < 10 ? warp - 2 : warp - 6;  // epilogue warp 0 .. kEpiWarps-1
     const int group = ew / 4;                          // handles weight tiles group, group + kEpiGroups, ...
-    uint16_t* buf = reinterpret_cast<uint16_t*>(epi) + ew * C::kEpiTok * 32;
+    uint16_t* buf = reinterpret_cast<uint16_t*>(epi) + ew * 32 * 32;   // FP32-scale epilogue only
     uint32_t acc = 0, acc_phase = 0;
     if constexpr (C::kF32) {
       // D[token, row] = sum_kb sB[e, nt, kb] * sA[token, kb] * partial_kb: promoted in FP32 registers,
@@ -798,30 +797,26 @@ __global__ void __launch_bounds__(Cfg<TOK, CPS, MAXE, FMT, WT>::kNumThreads, CPS
       // weight tile w of the item: accumulator columns w * TOK.., output columns (nt * WT + w) * 128..
       for (int w = group; w < WT; w += C::kEpiGroups) {
       const uint32_t taddr = tacc + w * TOK;
-      const int64_t dcol = static_cast<int64_t>(tl.nt * WT + w) * kBlockW + 32 * q + (lane & 3) * 8;
-      // chunk c0's 32 token columns -> bf16, transposed through shared memory, kEpiTok tokens at a
-      // time: buf[jj][lane] = D[token c0 + h + jj][weight row 32q + lane]
+      // chunk c0's 32 token columns -> bf16, stored straight from registers: lane l holds weight row
+      // 32q + l of every token; after one exchange with the neighbour lane, even lanes hold rows
+      // (l, l + 1) of token j and odd lanes rows (l - 1, l) of token j + 1, so each store writes 4
+      // bytes and a warp's store covers two tokens' 64-byte row segments.  (The earlier shared-memory
+      // transpose, 2-byte stores into a buffer then 16-byte loads and stores, cost 3-4 % of the
+      // large-M GEMMs: same-box A/B, bit-identical outputs.)
       auto emit = [&](const uint32_t (&r)[32], int c0) {
+        const int odd = lane & 1;
+        uint16_t* dst = p.d + static_cast<int64_t>(tl.tok0 + c0 + odd) * N +
+                        static_cast<int64_t>(tl.nt * WT + w) * kBlockW + 32 * q + (lane & ~1);
 #pragma unroll
-        for (int h = 0; h < 32; h += C::kEpiTok) {
-#pragma unroll
-          for (int jj = 0; jj < C::kEpiTok; ++jj) {
-            float v = __uint_as_float(r[h + jj]);
-            if constexpr (C::kFp4) v = v * alpha_a * alpha_b;
-            const __nv_bfloat16 hv = __float2bfloat16_rn(v);
-            buf[jj * 32 + lane] = *reinterpret_cast<const uint16_t*>(&hv);
+        for (int jj = 0; jj < 32; jj += 2) {
+          float v0 = __uint_as_float(r[jj]), v1 = __uint_as_float(r[jj + 1]);
+          if constexpr (C::kFp4) {
+            v0 = v0 * alpha_a * alpha_b;
+            v1 = v1 * alpha_a * alpha_b;
           }
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < C::kEpiTok / 8; ++i) {
-            const int jj = (lane >> 2) + 8 * i;
-            if (c0 + h + jj < tl.ntok) {
-              const uint4 v = *reinterpret_cast<const uint4*>(buf + jj * 32 + (lane & 3) * 8);
-              uint16_t* dst = p.d + static_cast<int64_t>(tl.tok0 + c0 + h + jj) * N + dcol;
-              *reinterpret_cast<uint4*>(dst) = v;
-            }
-          }
-          __syncwarp();
+          const float x = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+          const uint32_t pk = odd ? pack_bf16x2(x, v1) : pack_bf16x2(v0, x);
+          if (c0 + jj + odd < tl.ntok) *reinterpret_cast<uint32_t*>(dst + static_cast<int64_t>(jj) * N) = pk;
         }
       };
       // last chunk of the item in registers: hand the accumulator back to the MMA issuers
