@@ -30,8 +30,9 @@
 //   our 128-wide blocks use one byte for all four K-steps of a block: the
 //   int32 word holding four consecutive blocks is written to TMEM once per
 //   512 K and the byte is picked with sf_id = k_block % 4;
-// * epilogue: tcgen05.ld 32 columns (tokens) per thread row (weight row),
-//   transposed through shared memory into 64-byte row segments of D.
+// * epilogue: tcgen05.ld 32 columns (tokens) per thread row (weight row); after
+//   one exchange between neighbour lanes each lane stores two weight rows of one
+//   token (4 bytes), a warp's store covering two tokens' 64-byte row segments of D.
 #include "common.cuh"
 #include "host_utils.h"
 #include "tma_map.h"
@@ -95,8 +96,8 @@ struct GemmArgs {
 // into shared memory then cover 1.47x the MMA work of the 128 x 224 tile ((256 + 224) bytes per
 // 256 x 224 products against (128 + 224) per 128 x 224), which is what a latency-bound load
 // pipeline needs; the price is that the epilogue of one item no longer overlaps the next item's MMAs.
-// With at most 256 experts the items are 256 x 160 (kWideTok) instead: the smaller token tile, the
-// smaller tile tables and a half-size epilogue transpose buffer make room for a fourth stage, and
+// With at most 256 experts the items are 256 x 160 (kWideTok) instead: the smaller token tile and
+// the smaller tile tables make room for a fourth stage, and
 // with the load pipeline the limit (two MMA issuers keep the tensor core fed) the extra stage in
 // flight pays: same-box A/B, FP8 large gate-up 1713 -> 1534 us, large down 1020 -> 882 us, prefill
 // gate-up 378 -> 367 us; BF16 large gate-up 3160 -> 2826 us; outputs bit-identical.
