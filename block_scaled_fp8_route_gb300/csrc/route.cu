@@ -396,7 +396,9 @@ __global__ void __launch_bounds__(kThreads) route_fill_kernel(int E, int64_t m_c
 // read once, quantised with the arithmetic of quantise_act_kernel (quant_math.cuh, so the bytes are
 // the same), and its E4M3 codes and scale word are written to each of the token's k_r packed rows
 // (output_index from the assign kernel; -1 = dropped).  Launched as a programmatic dependent of the
-// routing kernels; only the loads of x are issued before the wait.
+// routing kernels: the loads of x and the quantisation run before the wait (x is complete before the
+// count kernel, a plain launch, starts; the assign kernel triggers this launch only after the count
+// kernel has completed), the reads of output_index and the stores after it.
 __global__ void __launch_bounds__(kThreads) quantise_scatter_kernel(const uint16_t* __restrict__ x, int64_t T,
                                                                     int64_t K, int kr,
                                                                     const int32_t* __restrict__ output_index,
@@ -417,9 +419,10 @@ __global__ void __launch_bounds__(kThreads) quantise_scatter_kernel(const uint16
     ra = __ldg(src);
     rb = __ldg(src + 1);
   }
-  pdl_wait();                                     // output_index is complete
-  if (!in_range) return;
-  const int dest_l = lane < kr ? output_index[t * kr + lane] : -1;
+  if (!in_range) {
+    pdl_wait();
+    return;
+  }
   float v[16];
   float amax = 0.f;
   if (active) {
@@ -454,6 +457,9 @@ __global__ void __launch_bounds__(kThreads) quantise_scatter_kernel(const uint16
   const uint32_t b2 = __shfl_sync(0xffffffffu, byte, 16);
   const uint32_t b3 = __shfl_sync(0xffffffffu, byte, 24);
   const int32_t word = static_cast<int32_t>(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24));
+  // the quantisation above needs nothing from the routing kernels; only the destinations do
+  pdl_wait();                                     // output_index is complete
+  const int dest_l = lane < kr ? output_index[t * kr + lane] : -1;
   for (int r = 0; r < kr; ++r) {
     const int dest = __shfl_sync(0xffffffffu, dest_l, r);   // warp-uniform
     if (dest < 0) continue;
