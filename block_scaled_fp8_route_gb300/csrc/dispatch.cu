@@ -151,6 +151,7 @@ bsf_status launch_dispatch(const void* x, int64_t T, int64_t K, const int32_t* t
   if (T < 0 || kr <= 0 || E <= 0 || K <= 0 || K % (FP4 ? 64 : 128)) return BSF_ERR_INVALID_ARGUMENT;
   if (layout != BSF_LAYOUT_CONTIGUOUS && layout != BSF_LAYOUT_MASKED) return BSF_ERR_INVALID_ARGUMENT;
   if (align_or_max_m < 1 || a_exp < -100 || a_exp > 100) return BSF_ERR_INVALID_ARGUMENT;
+  if (T > kSmallMaxR / kr) return BSF_ERR_UNSUPPORTED;   // before forming R, which must not wrap
   const int64_t R = T * kr;
   if (R > kSmallMaxR || E > kSmallMaxE) return BSF_ERR_UNSUPPORTED;
   if (!x || !topk_ids || !counts || !seg_start || !output_index || !token_of_row || !a_packed || !sfa_packed)
