@@ -85,6 +85,7 @@ extern "C" bsf_status bsf_combine(const void* y, int64_t y_rows, const int32_t* 
   if (T == 0) return BSF_OK;
   if (!y || !output_index || !topk_weights || !z) return BSF_ERR_INVALID_ARGUMENT;
   if (!aligned16(y) || !aligned16(z)) return BSF_ERR_MISALIGNED;
+  if (!fits_rows(T, N)) return BSF_ERR_UNSUPPORTED;
   const int64_t warps = T * ((N + 255) / 256);
   const int64_t blocks = (warps * 32 + 255) / 256;
   if (blocks > INT32_MAX) return BSF_ERR_UNSUPPORTED;

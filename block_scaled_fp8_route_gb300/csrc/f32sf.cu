@@ -121,6 +121,7 @@ extern "C" bsf_status bsf_quantise_act_f32sf(const void* x, int64_t T, int64_t K
   if (T == 0) return BSF_OK;
   if (!x || !q || !sf) return BSF_ERR_INVALID_ARGUMENT;
   if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return BSF_ERR_MISALIGNED;
+  if (!fits_rows(T, K)) return BSF_ERR_UNSUPPORTED;
   const int64_t blocks = (T * ((K + 511) / 512) * 32 + 255) / 256;
   if (blocks > INT32_MAX) return BSF_ERR_UNSUPPORTED;
   quantise_act_f32sf_kernel<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
@@ -134,6 +135,7 @@ extern "C" bsf_status bsf_quantise_weight_f32sf(const void* w, int64_t E, int64_
   if (E == 0) return BSF_OK;
   if (!w || !q || !sf) return BSF_ERR_INVALID_ARGUMENT;
   if (!aligned16(w) || !aligned16(q)) return BSF_ERR_MISALIGNED;
+  if (!fits_weights(E, N, K)) return BSF_ERR_UNSUPPORTED;
   const int64_t blocks = E * (N / 128) * (K / 128);
   if (blocks > INT32_MAX) return BSF_ERR_UNSUPPORTED;
   quantise_weight_f32sf_kernel<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(

@@ -12,6 +12,17 @@ namespace bsf {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Sizes beyond any real problem are refused (BSF_ERR_UNSUPPORTED) before a product of them is
+// formed, so no grid or offset computation can wrap: at most 2^31 - 1 rows (tokens, or experts x
+// rows) of at most 2^24 elements or bytes each.
+constexpr int64_t kMaxRows = INT32_MAX;
+constexpr int64_t kMaxRowWidth = int64_t(1) << 24;
+inline bool fits_rows(int64_t rows, int64_t width) { return rows <= kMaxRows && width <= kMaxRowWidth; }
+// E x N weight rows of width K
+inline bool fits_weights(int64_t E, int64_t N, int64_t K) {
+  return E <= kMaxRows && N <= kMaxRowWidth && fits_rows(E * N, K);
+}
+
 // Status of the launch just enqueued (configuration errors only; the kernel
 // itself runs asynchronously).
 inline bsf_status launch_status() {

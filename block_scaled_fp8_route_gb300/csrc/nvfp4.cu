@@ -119,6 +119,7 @@ extern "C" bsf_status bsf_quantise_act_nvfp4(const void* x, int64_t T, int64_t K
   if (T == 0) return BSF_OK;
   if (!x || !q || !sf) return BSF_ERR_INVALID_ARGUMENT;
   if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return BSF_ERR_MISALIGNED;
+  if (!fits_rows(T, K)) return BSF_ERR_UNSUPPORTED;
   return launch_quantise(x, T, K, T, a_exp, nullptr, q, sf, sf_ld, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -128,6 +129,7 @@ extern "C" bsf_status bsf_quantise_weight_nvfp4(const void* w, int64_t E, int64_
   if (E <= 0 || N <= 0 || K <= 0 || K % 64) return BSF_ERR_INVALID_ARGUMENT;
   if (!w || !b_exp || !q || !sfb) return BSF_ERR_INVALID_ARGUMENT;
   if (!aligned16(w) || !aligned16(q) || !aligned16(sfb)) return BSF_ERR_MISALIGNED;
+  if (!fits_weights(E, N, K)) return BSF_ERR_UNSUPPORTED;
   return launch_quantise(w, E * N, K, N, 0, b_exp, q, sfb, N, reinterpret_cast<cudaStream_t>(stream));
 }
 

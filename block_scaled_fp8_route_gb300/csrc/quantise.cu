@@ -175,6 +175,7 @@ extern "C" bsf_status bsf_tile_weights(const uint8_t* b, int64_t E, int64_t N, i
   if (E <= 0 || N <= 0 || row_bytes <= 0 || N % 128 || row_bytes % 128) return BSF_ERR_INVALID_ARGUMENT;
   if (!b || !out || b == out) return BSF_ERR_INVALID_ARGUMENT;
   if (!aligned16(b) || !aligned16(out)) return BSF_ERR_MISALIGNED;
+  if (!fits_weights(E, N, row_bytes)) return BSF_ERR_UNSUPPORTED;
   if (E * N > INT32_MAX || E * N * (row_bytes / 128) > INT32_MAX) return BSF_ERR_UNSUPPORTED;
   const int64_t n16 = E * N * row_bytes / 16;
   int64_t blocks = static_cast<int64_t>(sm_count()) * 8;
@@ -192,6 +193,7 @@ extern "C" bsf_status bsf_quantise_act(const void* x, int64_t T, int64_t K, uint
   if (!x || !q || !sf) return BSF_ERR_INVALID_ARGUMENT;
   if (sf_ld < T || sf_ld % 4 != 0) return BSF_ERR_INVALID_ARGUMENT;
   if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return BSF_ERR_MISALIGNED;
+  if (!fits_rows(T, K)) return BSF_ERR_UNSUPPORTED;
   const int64_t warps = T * ((K + 511) / 512);
   const int64_t blocks = (warps * 32 + 255) / 256;
   if (blocks > INT32_MAX) return BSF_ERR_UNSUPPORTED;
@@ -208,6 +210,7 @@ extern "C" bsf_status bsf_quantise_act_rows(const void* x, int64_t T, int64_t K,
   if (!x || !q || !sf || !token_of_row || !rows_used) return BSF_ERR_INVALID_ARGUMENT;
   if (sf_ld < T || sf_ld % 4 != 0) return BSF_ERR_INVALID_ARGUMENT;
   if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return BSF_ERR_MISALIGNED;
+  if (!fits_rows(T, K)) return BSF_ERR_UNSUPPORTED;
   const int64_t warps = T * ((K + 511) / 512);
   const int64_t blocks = (warps * 32 + 255) / 256;
   if (blocks > INT32_MAX) return BSF_ERR_UNSUPPORTED;
@@ -222,6 +225,7 @@ extern "C" bsf_status bsf_quantise_weight(const void* w, int64_t E, int64_t N, i
   if (E == 0) return BSF_OK;
   if (!w || !q || !sf128) return BSF_ERR_INVALID_ARGUMENT;
   if (!aligned16(w) || !aligned16(q)) return BSF_ERR_MISALIGNED;
+  if (!fits_weights(E, N, K)) return BSF_ERR_UNSUPPORTED;
   const int64_t blocks = E * (N / 128) * (K / 128);
   if (blocks > INT32_MAX) return BSF_ERR_UNSUPPORTED;
   quantise_weight_kernel<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
@@ -234,6 +238,7 @@ extern "C" bsf_status bsf_prepare_weight_sf(const float* sf128, int64_t E, int64
   if (E < 0 || N <= 0 || K <= 0 || N % 128 || K % 128) return BSF_ERR_INVALID_ARGUMENT;
   if (E == 0) return BSF_OK;
   if (!sf128 || !sfb) return BSF_ERR_INVALID_ARGUMENT;
+  if (!fits_weights(E, N, K)) return BSF_ERR_UNSUPPORTED;
   int* err = device_error_ptr();
   if (!err) return BSF_ERR_CUDA;
   const int64_t total = E * ((K / 128 + 3) / 4) * N;

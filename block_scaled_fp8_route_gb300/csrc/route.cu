@@ -677,6 +677,7 @@ extern "C" bsf_status bsf_route_quantise(const void* x, int64_t T, int64_t K, co
   if (kr > 32) return BSF_ERR_UNSUPPORTED;      // one lane per assignment of a token
   if (sfa_ld < m_cap || sfa_ld % 4) return BSF_ERR_INVALID_ARGUMENT;
   if (!aligned16(x) || !aligned16(a_packed) || !aligned16(sfa_packed)) return BSF_ERR_MISALIGNED;
+  if (!fits_rows(T, K)) return BSF_ERR_UNSUPPORTED;
   // routing, segment starts, padding marks and m_indices: bsf_route without a scatter source
   bsf_status st = bsf_route(topk_ids, T, kr, E, layout, align_or_max_m, counts, seg_start, output_index, token_of_row,
                             m_indices, m_cap, nullptr, nullptr, 0, K, nullptr, nullptr, 0, workspace, workspace_bytes,

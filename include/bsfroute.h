@@ -17,7 +17,10 @@
  *   - `stream` is a cudaStream_t (0 = legacy default stream).  All work is
  *     enqueued on it; calls never synchronise the device.
  *   - Arguments are validated on the host before anything is enqueued; a bad
- *     argument returns a non-zero bsf_status and enqueues nothing.
+ *     argument returns a non-zero bsf_status and enqueues nothing.  Sizes
+ *     beyond any real problem (more than 2^31 - 1 rows, tokens or experts x
+ *     weight rows, or rows wider than 2^24 elements or bytes) return
+ *     BSF_ERR_UNSUPPORTED before any product of them is formed.
  *   - Problems found while the kernels run (an expert id >= E, a masked slot
  *     overflow, a weight scale that is not a power of two, a wait that ran
  *     out) set bits of a sticky device error word; read it with

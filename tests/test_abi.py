@@ -209,3 +209,26 @@ def test_argument_validation_of_the_other_entry_points(lib):
     assert lib.bsf_checksum_u64(ok, 32, 0x2, ok, nul) == INVALID
     assert lib.bsf_checksum_u64(ok, 32, 0, nul, nul) == INVALID
     assert lib.bsf_checksum_u64(odd, 32, 0, ok, nul) == MISALIGNED
+
+
+def test_sizes_beyond_any_real_problem_are_refused_before_they_can_wrap(lib):
+    """Row counts above 2^31 - 1 or row widths above 2^24 return BSF_ERR_UNSUPPORTED before any product
+    of them is formed (T = 2^62 with K = 2^20 would wrap a 64-bit grid computation)."""
+    ok = ctypes.c_void_p(256)
+    nul = ctypes.c_void_p(0)
+    UNSUPPORTED = 3
+    T, K = 2**62, 2**20
+    assert lib.bsf_quantise_act(ok, T, K, ok, ok, T, nul) == UNSUPPORTED
+    assert lib.bsf_quantise_act_rows(ok, T, K, ok, ok, ok, ok, T, nul) == UNSUPPORTED
+    assert lib.bsf_quantise_act_f32sf(ok, T, K, ok, ok, T, nul) == UNSUPPORTED
+    assert lib.bsf_quantise_act_nvfp4(ok, T, K, 0, ok, ok, T, nul) == UNSUPPORTED
+    assert lib.bsf_quantise_act(ok, 64, 2**25, ok, ok, 64, nul) == UNSUPPORTED        # row wider than 2^24
+    assert lib.bsf_combine(ok, 8, ok, ok, T, 2, 1024, ok, nul) == UNSUPPORTED
+    assert lib.bsf_route_quantise(ok, T, K, ok, 1, 4, 0, 1, ok, ok, ok, ok, nul, 2**62, ok, ok, 2**62, ok, 64,
+                                  nul) == UNSUPPORTED
+    for E, N in ((2**40, 2**20), (2, 2**40)):
+        assert lib.bsf_quantise_weight(ok, E, N, 128, ok, ok, nul) == UNSUPPORTED
+        assert lib.bsf_quantise_weight_f32sf(ok, E, N, 128, ok, ok, nul) == UNSUPPORTED
+        assert lib.bsf_prepare_weight_sf(ok, E, N, 128, ok, nul) == UNSUPPORTED
+        assert lib.bsf_quantise_weight_nvfp4(ok, E, N, 128, ok, ok, ok, nul) == UNSUPPORTED
+        assert lib.bsf_tile_weights(ok, E, N, 128, ctypes.c_void_p(512), nul) == UNSUPPORTED
